@@ -1,0 +1,165 @@
+/*
+ * tts.h -- C ABI of libtts.so: tiled dense attention, deterministic top-k
+ * selection and permutation-invariant paged sparse attention for sm_103a.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named as device pointers must point to device memory of the
+ *   current CUDA device; sizes and scalars are host values. The caller owns
+ *   all memory. The library allocates nothing and keeps no state between
+ *   calls except a cached driver entry point.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *   entry point only enqueues work on that stream; none synchronises.
+ * - Host-side argument errors return a non-OK status and enqueue nothing.
+ *   A launch failure returns TTS_ERR_CUDA. Errors are never swallowed.
+ * - Values only the device can see (cu_seqlens, index lists, page tables,
+ *   top-k windows) are checked by the kernels: a bad entry is skipped (never
+ *   dereferenced) and a TTS_DEV_* bit is OR-ed into *dev_status when
+ *   dev_status is not NULL. Kernels never trap. A bounded wait that expires
+ *   sets TTS_DEV_TIMEOUT and the kernel returns early (its output is then
+ *   undefined). tts_status_from_device() turns a read-back word into a status.
+ * - No float atomics are used anywhere: for fixed inputs every output is
+ *   bitwise reproducible run to run.
+ */
+#ifndef TTS_H_
+#define TTS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TTS_OK = 0,
+  TTS_ERR_INVALID_ARG = 1,    /* null pointer, negative size, misaligned pointer, ... */
+  TTS_ERR_UNSUPPORTED = 2,    /* legal but not built (head_dim, head count, sizes) */
+  TTS_ERR_CUDA = 3,           /* a CUDA runtime / driver call or a launch failed */
+  TTS_ERR_INDEX_RANGE = 4,    /* device reported an out-of-range entry (skipped) */
+  TTS_ERR_DEVICE_TIMEOUT = 5, /* device reported an expired bounded wait */
+  TTS_ERR_WORKSPACE = 6       /* workspace missing or smaller than required */
+} tts_status;
+
+typedef enum { TTS_BF16 = 0, TTS_F32 = 1 } tts_dtype;
+
+/* Bits a kernel ORs into *dev_status. */
+#define TTS_DEV_INDEX_RANGE 0x1u
+#define TTS_DEV_TIMEOUT 0x2u
+#define TTS_DEV_BAD_ARG 0x4u
+
+const char* tts_status_string(int status);
+/* Map a dev_status word read back to the host onto a status (timeout wins). */
+int tts_status_from_device(uint32_t dev_status);
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tts_version(void);
+
+/*
+ * Dense attention forward over packed variable-length sequences.
+ *
+ * Follows the piece-wise attention of "DeepSeek V4.1 上 4×RTX 3090：视觉链路的两个坑
+ * 和修复" (section 三: S = Q_blk K^T, row softmax, P V, rows mapped back to the
+ * global rows of the block) and the varlen batch of "从 SGLang Kernel源码到 GPU
+ * Trace" (section 2.2: cu_seqlens_q / cu_seqlens_k; keys beyond a sequence's
+ * length are skipped, section 3.2), with FP32 softmax statistics and FP32
+ * accumulation ("AMD MI250部署DeepSeek-V4-Flash", sections 3.1 and 4.1) and the
+ * causal mask applied as -inf (section 3.3).
+ *
+ * For sequence b (tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q, and
+ * cu_seqlens_k[b] .. of k / v), query row i, head h, KV head g = h / (Hq/Hkv):
+ *   s_j = scale * q[i,h,:] . k[j,g,:]   for visible j: j < Lk and, if causal,
+ *                                       j <= i + (Lk - Lq)  (bottom-right)
+ *   out[i,h,:] = sum_j softmax(s)_j v[j,g,:]      lse[i,h] = ln sum_j e^{s_j}
+ * A row with no visible key gets out = 0, lse = -inf.
+ *
+ * q    device, [total_q, num_heads_q, head_dim], row-major, in_dtype
+ * k, v device, [total_k, num_heads_kv, head_dim], row-major, in_dtype
+ *      TTS_F32 inputs are rounded to bf16 (nearest-even) on the device first;
+ *      the MMAs always take bf16 operands and accumulate in fp32.
+ * cu_seqlens_q, cu_seqlens_k  device int32 [batch + 1], non-decreasing from 0,
+ *      last entry <= total_q / total_k (checked on the device: TTS_DEV_BAD_ARG,
+ *      offending sequences are skipped).
+ * max_seqlen_q, max_seqlen_k  host upper bounds of the sequence lengths (they
+ *      size the grid; a longer sequence is flagged TTS_DEV_BAD_ARG and skipped).
+ * head_dim   64, 80 or 128.    num_heads_q % num_heads_kv == 0.
+ * out  device fp32 [total_q, num_heads_q, head_dim]; lse device fp32
+ *      [total_q, num_heads_q] (may be NULL). Rows of q not covered by any
+ *      sequence are left untouched.
+ * workspace  device scratch of at least tts_attn_workspace_bytes(...) bytes
+ *      (16-byte aligned); may be NULL when that size is 0.
+ * q, k, v must be 16-byte aligned.
+ */
+size_t tts_attn_workspace_bytes(int64_t total_q, int64_t total_k, int32_t num_heads_q,
+                                int32_t num_heads_kv, int32_t head_dim, tts_dtype in_dtype);
+
+tts_status tts_attn_fwd_varlen(const void* q, const void* k, const void* v, tts_dtype in_dtype,
+                               int64_t total_q, int64_t total_k, const int32_t* cu_seqlens_q,
+                               const int32_t* cu_seqlens_k, int32_t batch, int32_t max_seqlen_q,
+                               int32_t max_seqlen_k, int32_t num_heads_q, int32_t num_heads_kv,
+                               int32_t head_dim, int32_t causal, float scale, float* out,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               uint32_t* dev_status, void* stream);
+
+/*
+ * Deterministic top-k selection over per-row indexer logits.
+ *
+ * Follows "推理引擎的蝴蝶效应 -- 从V32 模型的输出不一致说起" (section 实验方法和
+ * 结果: logits (323, 2590) with row_starts / row_lens give top-k indices
+ * (323, 2048); a stable sort replaces the unstable top-k) and the fixed
+ * tie-break rule of "AMD MI250部署DeepSeek-V4-Flash" (section 4.2).
+ *
+ * Row r's window is logits[r * row_stride + row_starts[r] .. + row_lens[r]).
+ * idx[r, 0 .. min(k, len)) = window positions (relative to row_starts[r])
+ * ordered by value descending, equal values by ascending position (lower
+ * index wins); remaining slots are -1. Values compare as floats (-0 == +0).
+ * NaN logits are not supported (their rank is unspecified).
+ * A window that does not fit in the row sets TTS_DEV_INDEX_RANGE and yields
+ * an all -1 row.
+ *
+ * logits   device fp32 [rows, row_stride]
+ * row_starts, row_lens  device int32 [rows]
+ * idx      device int32 [rows, k]
+ * Limits: 1 <= k <= 4096, 1 <= row_stride <= 16384 (TTS_ERR_UNSUPPORTED otherwise).
+ */
+tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows,
+                           const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                           int32_t* idx, uint32_t* dev_status, void* stream);
+
+/*
+ * Sparse attention over a paged KV cache, invariant to the order of the index list.
+ *
+ * Follows "推理引擎的蝴蝶效应 -- 从V32 模型的输出不一致说起" (section 实验方法和
+ * 结果: the KV rows are fetched through pagetable_1 and sorting the index list
+ * makes outputs identical; section 进一步探索, equations 1-2: the online-softmax
+ * merge whose rounding depends on block order). The kernel sorts each query's
+ * index list ascending before attending, so any permutation of idx[n, :] gives
+ * bitwise identical out / lse.
+ *
+ * For query n and head h: the valid entries i of idx[n, :] (0 <= i < kv_len,
+ * page_table[i / page_size] in [0, num_pages)), sorted ascending, duplicates
+ * kept; row_i = kv_cache[page_table[i / page_size], i % page_size, :];
+ *   s_i = scale * q[n,h,:] . row_i[0:dqk]
+ *   out[n,h,:] = sum_i softmax(s)_i row_i[0:dv]     lse[n,h] = ln sum_i e^{s_i}
+ * Entries equal to -1 are empty slots. Other invalid entries are skipped and set
+ * TTS_DEV_INDEX_RANGE. A query with no valid entry gets out = 0, lse = -inf.
+ *
+ * q          device bf16 [nq, num_heads, dqk]
+ * kv_cache   device bf16 [num_pages, page_size, dqk]  (V = the first dv columns)
+ * page_table device int32 [num_logical_pages]
+ * idx        device int32 [nq, topk]
+ * out        device fp32 [nq, num_heads, dv];  lse device fp32 [nq, num_heads] or NULL
+ * Built shape: num_heads = 128, dqk = 576, dv = 512, 1 <= topk <= 4096,
+ * page_size >= 1 (TTS_ERR_UNSUPPORTED otherwise). q and kv_cache 16-byte aligned.
+ */
+tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, int32_t dqk,
+                                 int32_t dv, const void* kv_cache, int32_t num_pages,
+                                 int32_t page_size, const int32_t* page_table,
+                                 int32_t num_logical_pages, int32_t kv_len, const int32_t* idx,
+                                 int32_t topk, float scale, float* out, float* lse,
+                                 uint32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTS_H_ */

@@ -1,0 +1,120 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports every
+function tts.h declares, and rejects bad host-side arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from tiled_top_sparse_gb300 import _build
+    _build.build()
+    import tiled_top_sparse_gb300 as tts
+    return tts.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tts.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tts_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(L, n), f"libtts.so does not export {n}"
+    import tiled_top_sparse_gb300 as tts
+    assert set(names) == set(tts.EXPORTED)
+
+
+def test_status_strings_and_device_mapping(L):
+    import tiled_top_sparse_gb300 as tts
+    assert tts.status_string(0) == "ok"
+    for c in range(1, 7):
+        assert tts.status_string(c) not in ("ok", "unknown status")
+    f = L.tts_status_from_device
+    assert f(0) == tts.TTS_OK
+    assert f(tts.TTS_DEV_INDEX_RANGE) == tts.TTS_ERR_INDEX_RANGE
+    assert f(tts.TTS_DEV_TIMEOUT | tts.TTS_DEV_INDEX_RANGE) == tts.TTS_ERR_DEVICE_TIMEOUT
+    assert f(tts.TTS_DEV_BAD_ARG) == tts.TTS_ERR_INVALID_ARG
+    assert L.tts_version() >= 100
+
+
+def test_workspace_size(L):
+    import tiled_top_sparse_gb300 as tts
+    assert L.tts_attn_workspace_bytes(256, 256, 1, 1, 64, tts.TTS_BF16) == 0
+    n = L.tts_attn_workspace_bytes(256, 256, 1, 1, 64, tts.TTS_F32)
+    assert n >= 3 * 256 * 64 * 2
+
+
+# Fake, never-dereferenced pointers: host validation must reject before any CUDA call.
+P = ctypes.c_void_p(0x1000)
+NUL = None
+
+
+def test_topk_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    f = L.tts_topk_select
+    assert f(NUL, 10, 1, P, P, 4, P, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 10, 1, P, P, 0, P, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 0, 1, P, P, 4, P, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 10, -1, P, P, 4, P, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 10, 1, P, P, 4097, P, NUL, NUL) == tts.TTS_ERR_UNSUPPORTED
+    assert f(P, 16385, 1, P, P, 16, P, NUL, NUL) == tts.TTS_ERR_UNSUPPORTED
+    assert f(P, 10, 0, P, P, 4, P, NUL, NUL) == tts.TTS_OK  # nothing to do
+
+
+def _attn(L, **kw):
+    a = dict(q=P, k=P, v=P, dt=0, tq=256, tk=256, cq=P, ck=P, b=1, mq=256, mk=256, hq=2, hkv=1,
+             d=64, causal=0, scale=0.125, out=P, lse=NUL, ws=NUL, wsb=0, st=NUL, stream=NUL)
+    a.update(kw)
+    return L.tts_attn_fwd_varlen(*a.values())
+
+
+def test_attn_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    assert _attn(L, q=NUL) == tts.TTS_ERR_INVALID_ARG
+    assert _attn(L, hq=3, hkv=2) == tts.TTS_ERR_INVALID_ARG
+    assert _attn(L, scale=0.0) == tts.TTS_ERR_INVALID_ARG
+    assert _attn(L, scale=float("nan")) == tts.TTS_ERR_INVALID_ARG
+    assert _attn(L, causal=2) == tts.TTS_ERR_INVALID_ARG
+    assert _attn(L, b=0) == tts.TTS_ERR_INVALID_ARG
+    assert _attn(L, dt=7) == tts.TTS_ERR_INVALID_ARG
+    assert _attn(L, d=96) == tts.TTS_ERR_UNSUPPORTED
+    assert _attn(L, q=ctypes.c_void_p(0x1008)) == tts.TTS_ERR_INVALID_ARG  # misaligned
+    assert _attn(L, dt=1) == tts.TTS_ERR_WORKSPACE  # fp32 needs a workspace
+    assert _attn(L, tq=0) == tts.TTS_OK
+
+
+def _sparse(L, **kw):
+    a = dict(q=P, nq=4, H=128, dqk=576, dv=512, kv=P, pages=41, ps=64, pt=P, nlp=41, kv_len=2590,
+             idx=P, topk=2048, scale=0.04, out=P, lse=NUL, st=NUL, stream=NUL)
+    a.update(kw)
+    return L.tts_sparse_attn_paged(*a.values())
+
+
+def test_sparse_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    assert _sparse(L, q=NUL) == tts.TTS_ERR_INVALID_ARG
+    assert _sparse(L, idx=NUL) == tts.TTS_ERR_INVALID_ARG
+    assert _sparse(L, topk=0) == tts.TTS_ERR_INVALID_ARG
+    assert _sparse(L, dv=600) == tts.TTS_ERR_INVALID_ARG
+    assert _sparse(L, ps=0) == tts.TTS_ERR_INVALID_ARG
+    assert _sparse(L, scale=-1.0) == tts.TTS_ERR_INVALID_ARG
+    assert _sparse(L, H=64) == tts.TTS_ERR_UNSUPPORTED
+    assert _sparse(L, topk=4097) == tts.TTS_ERR_UNSUPPORTED
+    assert _sparse(L, nq=0) == tts.TTS_OK
+
+
+def test_product_has_no_cpu_fallback():
+    """The binding must not import the oracle or any CPU path."""
+    pkg = os.path.join(ROOT, "tiled_top_sparse_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert "import oracle" not in src and "from oracle" not in src, fn

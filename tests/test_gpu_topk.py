@@ -1,0 +1,87 @@
+"""GPU parity for tts_topk_select: indices bit-exact against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tts():
+    import tiled_top_sparse_gb300 as m
+    m.lib()
+    return m
+
+
+def run(tts, inp: W.TopkInputs, status=None):
+    dev = torch.device("cuda")
+    return tts.topk_select(inp.logits.to(dev), inp.row_starts.to(dev), inp.row_lens.to(dev),
+                           inp.k, status=status)
+
+
+def oracle_idx(inp):
+    idx, bad = oracle.topk(inp.logits.numpy(), inp.row_starts.numpy(), inp.row_lens.numpy(),
+                           inp.k)
+    return idx, bad
+
+
+def test_full_config_bit_exact_and_repeatable(tts):
+    inp = W.topk_inputs()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = run(tts, inp, st)
+    b = run(tts, inp, st)
+    ref, bad = oracle_idx(inp)
+    assert bad == 0
+    tts.check_status(st)
+    assert np.array_equal(a.cpu().numpy(), ref)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("rows,cols,k", [(7, 100, 16), (33, 5000, 4096), (5, 16384, 3000),
+                                         (40, 700, 1), (3, 2049, 2048)])
+def test_shapes_with_ties(tts, rows, cols, k):
+    inp = W.topk_inputs(rows=rows, cols=cols, k=k, seed=rows * 7 + k, causal=True)
+    ref, _ = oracle_idx(inp)
+    assert np.array_equal(run(tts, inp).cpu().numpy(), ref)
+
+
+def test_heavy_ties_and_signed_zero(tts):
+    g = torch.Generator().manual_seed(9)
+    x = torch.randint(-2, 3, (16, 3000), generator=g).float()
+    x[x == 0] = torch.where(torch.rand(int((x == 0).sum()), generator=g) < 0.5,
+                            torch.tensor(0.0), torch.tensor(-0.0))
+    inp = W.TopkInputs(x, torch.zeros(16, dtype=torch.int32),
+                       torch.full((16,), 3000, dtype=torch.int32), 2048)
+    ref, _ = oracle_idx(inp)
+    assert np.array_equal(run(tts, inp).cpu().numpy(), ref)
+
+
+def test_short_rows_offsets_and_bad_windows(tts):
+    g = torch.Generator().manual_seed(10)
+    x = torch.randn(6, 3000, generator=g).to(torch.bfloat16).float()
+    starts = torch.tensor([0, 100, 2999, 5, -1, 10], dtype=torch.int32)
+    lens = torch.tensor([0, 50, 1, 2990, 10, 2995], dtype=torch.int32)  # rows 4, 5 invalid
+    inp = W.TopkInputs(x, starts, lens, 2048)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run(tts, inp, st).cpu().numpy()
+    ref, bad = oracle_idx(inp)
+    assert bad == 2
+    assert np.array_equal(got, ref)
+    assert int(st.item()) & tts.TTS_DEV_INDEX_RANGE
+    with pytest.raises(tts.TTSError):
+        tts.check_status(st)
+
+
+def test_output_canaries_untouched(tts):
+    inp = W.topk_inputs(rows=20, cols=2590, k=2048, seed=11)
+    dev = torch.device("cuda")
+    buf = torch.full((20 * 2048 + 2 * 4096,), -12345, dtype=torch.int32, device=dev)
+    idx = buf[4096:4096 + 20 * 2048].view(20, 2048)
+    tts.topk_select(inp.logits.to(dev), inp.row_starts.to(dev), inp.row_lens.to(dev), 2048, idx=idx)
+    torch.cuda.synchronize()
+    assert bool((buf[:4096] == -12345).all()) and bool((buf[-4096:] == -12345).all())
+    ref, _ = oracle_idx(inp)
+    assert np.array_equal(idx.cpu().numpy(), ref)

@@ -1,0 +1,214 @@
+"""Thin Python binding over libtts.so (the C ABI declared in include/tts.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels. PyTorch supplies device memory and the current stream. There is
+no fallback: if the library is missing or fails to load, calls raise.
+
+    attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    causal, scale, out=None, lse=None, workspace=None, status=None)
+    topk_select(logits, row_starts, row_lens, k, idx=None, status=None)
+    sparse_attn_paged(q, kv_cache, page_table, idx, kv_len, scale, dv=512,
+                      out=None, lse=None, status=None)
+
+`status`, when given, is a 1-element int32 CUDA tensor the kernels OR their
+device-side flags into (see TTS_DEV_* in the header); `check_status(status)`
+synchronises and raises on a set flag.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtts.so")
+
+TTS_OK = 0
+TTS_ERR_INVALID_ARG = 1
+TTS_ERR_UNSUPPORTED = 2
+TTS_ERR_CUDA = 3
+TTS_ERR_INDEX_RANGE = 4
+TTS_ERR_DEVICE_TIMEOUT = 5
+TTS_ERR_WORKSPACE = 6
+TTS_BF16 = 0
+TTS_F32 = 1
+TTS_DEV_INDEX_RANGE = 0x1
+TTS_DEV_TIMEOUT = 0x2
+TTS_DEV_BAD_ARG = 0x4
+
+EXPORTED = (
+    "tts_status_string",
+    "tts_status_from_device",
+    "tts_version",
+    "tts_attn_workspace_bytes",
+    "tts_attn_fwd_varlen",
+    "tts_topk_select",
+    "tts_sparse_attn_paged",
+)
+
+
+class TTSError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtts.so (built by tiled_top_sparse_gb300._build). Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libtts.so not built ({LIB_PATH}); run tiled_top_sparse_gb300/_build.py")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    L.tts_status_string.argtypes = [ctypes.c_int]
+    L.tts_status_string.restype = ctypes.c_char_p
+    L.tts_status_from_device.argtypes = [ctypes.c_uint32]
+    L.tts_status_from_device.restype = ctypes.c_int
+    L.tts_version.argtypes = []
+    L.tts_version.restype = ctypes.c_int
+    L.tts_attn_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, ctypes.c_int]
+    L.tts_attn_workspace_bytes.restype = ctypes.c_size_t
+    L.tts_attn_fwd_varlen.argtypes = [P, P, P, ctypes.c_int, i64, i64, P, P, i32, i32, i32, i32,
+                                      i32, i32, i32, f32, P, P, P, ctypes.c_size_t, P, P]
+    L.tts_attn_fwd_varlen.restype = ctypes.c_int
+    L.tts_topk_select.argtypes = [P, i64, i32, P, P, i32, P, P, P]
+    L.tts_topk_select.restype = ctypes.c_int
+    L.tts_sparse_attn_paged.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, i32, i32, P, i32,
+                                        f32, P, P, P, P]
+    L.tts_sparse_attn_paged.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().tts_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != TTS_OK:
+        raise TTSError(code, what)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(t: torch.Tensor, name: str, dtype=None):
+    _need(isinstance(t, torch.Tensor) and t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def check_status(status: torch.Tensor, what: str = "device status"):
+    """Synchronise on `status` (1-element int32 CUDA tensor) and raise if a flag is set."""
+    v = int(status.item()) & 0xFFFFFFFF
+    _check(lib().tts_status_from_device(ctypes.c_uint32(v)), what)
+
+
+def attn_workspace_bytes(total_q, total_k, num_heads_q, num_heads_kv, head_dim, dtype) -> int:
+    code = TTS_F32 if dtype == torch.float32 else TTS_BF16
+    return int(lib().tts_attn_workspace_bytes(int(total_q), int(total_k), int(num_heads_q),
+                                              int(num_heads_kv), int(head_dim), code))
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal,
+                    scale, out=None, lse=None, workspace=None, status=None, want_lse=True):
+    """Dense attention forward over packed varlen sequences (tts_attn_fwd_varlen).
+
+    q [total_q, Hq, d], k/v [total_k, Hkv, d] (bf16 or fp32, same dtype), cu_seqlens_* int32
+    [batch+1] on the device. Returns (out fp32 [total_q, Hq, d], lse fp32 [total_q, Hq]).
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _cuda_contig(t, n)
+        _need(t.dim() == 3, f"{n} must be [tokens, heads, head_dim]")
+    _need(q.dtype == k.dtype == v.dtype and q.dtype in (torch.bfloat16, torch.float32),
+          "q, k, v must share dtype bf16 or fp32")
+    _need(k.shape == v.shape, "k and v must have the same shape")
+    _cuda_contig(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _cuda_contig(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+    total_q, hq, d = q.shape
+    total_k, hkv, d2 = k.shape
+    _need(d == d2, "head_dim mismatch")
+    batch = cu_seqlens_q.numel() - 1
+    _need(batch >= 1 and cu_seqlens_k.numel() == batch + 1, "cu_seqlens sizes must be batch+1")
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=torch.float32, device=q.device)
+    _cuda_contig(out, "out", torch.float32)
+    _need(tuple(out.shape) == (total_q, hq, d), "out shape")
+    if lse is None and want_lse:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _cuda_contig(lse, "lse", torch.float32)
+    dt = TTS_F32 if q.dtype == torch.float32 else TTS_BF16
+    need = attn_workspace_bytes(total_q, total_k, hq, hkv, d, q.dtype)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().tts_attn_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), dt, total_q, total_k, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        batch, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d, int(bool(causal)), float(scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(q.device))
+    _check(code, "tts_attn_fwd_varlen")
+    return out, lse
+
+
+def topk_select(logits, row_starts, row_lens, k, idx=None, status=None):
+    """Deterministic per-row top-k (tts_topk_select). Returns idx int32 [rows, k]."""
+    _cuda_contig(logits, "logits", torch.float32)
+    _need(logits.dim() == 2, "logits must be [rows, row_stride]")
+    _cuda_contig(row_starts, "row_starts", torch.int32)
+    _cuda_contig(row_lens, "row_lens", torch.int32)
+    rows, stride = logits.shape
+    _need(row_starts.numel() == rows and row_lens.numel() == rows, "row_starts/row_lens size")
+    if idx is None:
+        idx = torch.empty((rows, int(k)), dtype=torch.int32, device=logits.device)
+    _cuda_contig(idx, "idx", torch.int32)
+    _need(tuple(idx.shape) == (rows, int(k)), "idx shape")
+    code = lib().tts_topk_select(_ptr(logits), stride, rows, _ptr(row_starts), _ptr(row_lens),
+                                 int(k), _ptr(idx), _ptr(status), _stream(logits.device))
+    _check(code, "tts_topk_select")
+    return idx
+
+
+def sparse_attn_paged(q, kv_cache, page_table, idx, kv_len, scale, dv=512, out=None, lse=None,
+                      status=None, want_lse=True):
+    """Order-invariant sparse attention through a page table (tts_sparse_attn_paged).
+
+    q bf16 [nq, H, dqk], kv_cache bf16 [pages, page_size, dqk], page_table int32 [n_pages],
+    idx int32 [nq, topk]. Returns (out fp32 [nq, H, dv], lse fp32 [nq, H]).
+    """
+    _cuda_contig(q, "q", torch.bfloat16)
+    _cuda_contig(kv_cache, "kv_cache", torch.bfloat16)
+    _cuda_contig(page_table, "page_table", torch.int32)
+    _cuda_contig(idx, "idx", torch.int32)
+    _need(q.dim() == 3 and kv_cache.dim() == 3 and idx.dim() == 2, "ranks")
+    nq, H, dqk = q.shape
+    pages, page_size, dk2 = kv_cache.shape
+    _need(dk2 == dqk and idx.shape[0] == nq, "shapes")
+    if out is None:
+        out = torch.empty((nq, H, dv), dtype=torch.float32, device=q.device)
+    _cuda_contig(out, "out", torch.float32)
+    if lse is None and want_lse:
+        lse = torch.empty((nq, H), dtype=torch.float32, device=q.device)
+    code = lib().tts_sparse_attn_paged(
+        _ptr(q), nq, H, dqk, int(dv), _ptr(kv_cache), pages, page_size, _ptr(page_table),
+        page_table.numel(), int(kv_len), _ptr(idx), idx.shape[1], float(scale), _ptr(out),
+        _ptr(lse), _ptr(status), _stream(q.device))
+    _check(code, "tts_sparse_attn_paged")
+    return out, lse

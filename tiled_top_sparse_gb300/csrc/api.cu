@@ -1,0 +1,220 @@
+// C ABI of libtts.so: host-side argument validation, workspace carving and
+// launches. Every check that needs only host values happens here, before any
+// work is enqueued; values that live on the device are checked in the kernels.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/tts.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tts {
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
+                           void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                           const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t d[5];
+  cuuint64_t s[4];
+  cuuint32_t bx[5], es[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  return g_encode(map, dtype, rank, base, d, s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace tts
+
+using namespace tts;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline tts_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return TTS_OK;
+  if (e == cudaErrorInvalidValue) return TTS_ERR_INVALID_ARG;
+  return TTS_ERR_CUDA;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* tts_status_string(int status) {
+  switch (status) {
+    case TTS_OK: return "ok";
+    case TTS_ERR_INVALID_ARG: return "invalid argument";
+    case TTS_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case TTS_ERR_CUDA: return "CUDA error";
+    case TTS_ERR_INDEX_RANGE: return "device reported an out-of-range index (entry skipped)";
+    case TTS_ERR_DEVICE_TIMEOUT: return "device reported an expired bounded wait";
+    case TTS_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int tts_status_from_device(uint32_t dev_status) {
+  if (dev_status & TTS_DEV_TIMEOUT) return TTS_ERR_DEVICE_TIMEOUT;
+  if (dev_status & TTS_DEV_BAD_ARG) return TTS_ERR_INVALID_ARG;
+  if (dev_status & TTS_DEV_INDEX_RANGE) return TTS_ERR_INDEX_RANGE;
+  return TTS_OK;
+}
+
+int tts_version(void) { return 100; }
+
+size_t tts_attn_workspace_bytes(int64_t total_q, int64_t total_k, int32_t num_heads_q,
+                                int32_t num_heads_kv, int32_t head_dim, tts_dtype in_dtype) {
+  if (in_dtype != TTS_F32 || total_q < 0 || total_k < 0 || num_heads_q < 1 || num_heads_kv < 1 ||
+      head_dim < 1)
+    return 0;
+  const size_t nq = (size_t)total_q * num_heads_q * head_dim * 2;
+  const size_t nk = (size_t)total_k * num_heads_kv * head_dim * 2;
+  return align_up(nq, 256) + 2 * align_up(nk, 256);
+}
+
+tts_status tts_attn_fwd_varlen(const void* q, const void* k, const void* v, tts_dtype in_dtype,
+                               int64_t total_q, int64_t total_k, const int32_t* cu_seqlens_q,
+                               const int32_t* cu_seqlens_k, int32_t batch, int32_t max_seqlen_q,
+                               int32_t max_seqlen_k, int32_t num_heads_q, int32_t num_heads_kv,
+                               int32_t head_dim, int32_t causal, float scale, float* out,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               uint32_t* dev_status, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || cu_seqlens_q == nullptr ||
+      cu_seqlens_k == nullptr || out == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (in_dtype != TTS_BF16 && in_dtype != TTS_F32) return TTS_ERR_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+      num_heads_q < 1 || num_heads_kv < 1 || head_dim < 1)
+    return TTS_ERR_INVALID_ARG;
+  if (num_heads_q % num_heads_kv != 0) return TTS_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return TTS_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return TTS_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 80 && head_dim != 128) return TTS_ERR_UNSUPPORTED;
+  if (total_q > 0x7FFFFF00LL || total_k > 0x7FFFFF00LL) return TTS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return TTS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (total_q == 0 || max_seqlen_q == 0) return TTS_OK;  // nothing to compute
+
+  AttnArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  if (in_dtype == TTS_F32) {
+    const size_t need =
+        tts_attn_workspace_bytes(total_q, total_k, num_heads_q, num_heads_kv, head_dim, in_dtype);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+      return TTS_ERR_WORKSPACE;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    const int64_t nq = total_q * num_heads_q * head_dim;
+    const int64_t nk = total_k * num_heads_kv * head_dim;
+    void* qb = w;
+    void* kb = w + align_up((size_t)nq * 2, 256);
+    void* vb = static_cast<uint8_t*>(kb) + align_up((size_t)nk * 2, 256);
+    cudaError_t e = launch_f32_to_bf16(static_cast<const float*>(q), qb, nq, st);
+    if (e == cudaSuccess) e = launch_f32_to_bf16(static_cast<const float*>(k), kb, nk, st);
+    if (e == cudaSuccess) e = launch_f32_to_bf16(static_cast<const float*>(v), vb, nk, st);
+    if (e != cudaSuccess) return TTS_ERR_CUDA;
+    a.q = qb;
+    a.k = kb;
+    a.v = vb;
+  }
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.batch = batch;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.hq = num_heads_q;
+  a.hkv = num_heads_kv;
+  a.d = head_dim;
+  a.causal = causal;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  int drv = 0;
+  cudaError_t e = launch_attn_fwd(a, &drv, st);
+  if (drv != 0) return TTS_ERR_CUDA;
+  return from_cuda(e);
+}
+
+tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows,
+                           const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                           int32_t* idx, uint32_t* dev_status, void* stream) {
+  if (logits == nullptr || row_starts == nullptr || row_lens == nullptr || idx == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (rows < 0 || row_stride < 1 || k < 1) return TTS_ERR_INVALID_ARG;
+  if (k > 4096 || row_stride > 16384) return TTS_ERR_UNSUPPORTED;
+  if (rows == 0) return TTS_OK;
+  return from_cuda(launch_topk_select(logits, row_stride, rows, row_starts, row_lens, k, idx,
+                                      dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, int32_t dqk,
+                                 int32_t dv, const void* kv_cache, int32_t num_pages,
+                                 int32_t page_size, const int32_t* page_table,
+                                 int32_t num_logical_pages, int32_t kv_len, const int32_t* idx,
+                                 int32_t topk, float scale, float* out, float* lse,
+                                 uint32_t* dev_status, void* stream) {
+  if (q == nullptr || kv_cache == nullptr || page_table == nullptr || idx == nullptr ||
+      out == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (nq < 0 || num_heads < 1 || dqk < 1 || dv < 1 || dv > dqk || num_pages < 1 ||
+      page_size < 1 || num_logical_pages < 0 || kv_len < 0 || topk < 1)
+    return TTS_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return TTS_ERR_INVALID_ARG;
+  if ((int64_t)num_pages * page_size > 0x7FFFFF00LL) return TTS_ERR_UNSUPPORTED;
+  if (num_heads != 128 || dqk != 576 || dv != 512 || topk > 4096) return TTS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return TTS_ERR_INVALID_ARG;
+  if (nq == 0) return TTS_OK;
+  SparseArgs a;
+  a.q = q;
+  a.kv_cache = kv_cache;
+  a.page_table = page_table;
+  a.idx = idx;
+  a.nq = nq;
+  a.heads = num_heads;
+  a.dqk = dqk;
+  a.dv = dv;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.num_logical_pages = num_logical_pages;
+  a.kv_len = kv_len;
+  a.topk = topk;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  int drv = 0;
+  cudaError_t e = launch_sparse_attn(a, &drv, static_cast<cudaStream_t>(stream));
+  if (drv != 0) return TTS_ERR_CUDA;
+  return from_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,483 @@
+// Dense attention forward (non-causal vision and varlen causal GQA prefill).
+//
+// What it computes: for every query row, softmax(scale * q K^T) V over the
+// visible keys, plus lse = ln sum exp(scale * q k) -- the S-gemm / softmax /
+// PV-gemm pieces of "DeepSeek V4.1 上 4×RTX 3090" (section 三), over the
+// cu_seqlens batches of "从 SGLang Kernel源码到 GPU Trace" (section 2.2, keys past
+// a sequence's length skipped as in section 3.2), FP32 statistics and FP32
+// accumulation as in "AMD MI250部署DeepSeek-V4-Flash" (3.1, 4.1), causal mask
+// as -inf (3.3), and the online-softmax merge of "推理引擎的蝴蝶效应" (进一步探索,
+// equations 1-2) applied tile after tile in a fixed order.
+//
+// How (one CTA = one (sequence, 256-row query pair, head)):
+//   warp 0        TMA producer: Q tiles once, then K/V 128-row tiles into a ring
+//   warp 1        TMEM allocator + single-thread tcgen05 MMA issuer
+//   warps 4..7    softmax warpgroup 0 (query rows 0..127 of the pair)
+//   warps 8..11   softmax warpgroup 1 (query rows 128..255)
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D).
+// S = Q K^T lands in TMEM; each softmax thread owns one row (TMEM lane), keeps
+// the running max / sum in fp32 registers, writes P as bf16 pairs over the first
+// 64 columns of its S region, and the MMA warp issues O += P V with P read
+// straight from TMEM. The two warpgroups ping-pong so the tensor core works
+// on one tile's MMAs while the other tile's softmax runs.
+// The running max is only moved (and O rescaled) when it grows by more than
+// 2^8 in the exp2 domain; otherwise P uses the older max, which bounds P by
+// 256 and is exact in real arithmetic (the final O / l cancels the offset).
+// No S or P matrix ever touches global memory, so there is no piece buffer
+// to index (the q0*N overflow of the vision write-up cannot happen here).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tts {
+namespace {
+
+constexpr int kAttnThreads = 384;
+constexpr int kBlockM = 128;  // query rows per softmax warpgroup
+constexpr int kBlockN = 128;  // keys per K/V tile
+
+template <int D>
+struct AttnCfg {
+  static constexpr int kMainBoxes = D / 64;  // 64-column SW128 boxes
+  static constexpr int kTail = D % 64;       // 0 or 16 (SW32 box)
+  static constexpr int kBoxBytes = kBlockN * 128;  // one SW128 box of 128 rows
+  static constexpr int kTailBytes = kBlockN * 32;  // one SW32 box of 128 rows
+  static constexpr int kTileBytes = kMainBoxes * kBoxBytes + (kTail ? kTailBytes : 0);
+  static constexpr int kStages = (D <= 80) ? 3 : 2;
+  static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
+  static_assert(kTail == 0 || kTail == 16, "head_dim must be 64, 80 or 128");
+};
+
+struct AttnMaps {
+  CUtensorMap q, k, v;           // SW128 boxes {64, 1, 128}
+  CUtensorMap q_t, k_t, v_t;     // SW32 boxes {16, 1, 128} for the d=64..79 tail
+};
+
+struct AttnParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  float* out;
+  float* lse;
+  uint32_t* dev_status;
+  int64_t total_q, total_k;
+  int batch, max_seqlen_q, max_seqlen_k, hq, hkv, causal, pairs_max;
+  float scale, scale_log2;
+};
+
+// Load one 128-row tile (all boxes) of a [tokens, heads, D] tensor.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* main,
+                                          const CUtensorMap* tail, uint32_t bar, int head,
+                                          int token) {
+  using C = AttnCfg<D>;
+#pragma unroll
+  for (int b = 0; b < C::kMainBoxes; ++b)
+    tma_load_3d(dst + b * C::kBoxBytes, main, bar, b * 64, head, token);
+  if constexpr (C::kTail != 0)
+    tma_load_3d(dst + C::kMainBoxes * C::kBoxBytes, tail, bar, C::kMainBoxes * 64, head, token);
+}
+
+// S[tmem] = Q[smem] K[smem]^T over the D-deep contraction.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_s, uint32_t k_s) {
+  using C = AttnCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32(128, kBlockN, 0, 0);
+#pragma unroll
+  for (int ks = 0; ks < C::kMainBoxes * 4; ++ks) {
+    const uint32_t off = (ks / 4) * C::kBoxBytes + (ks % 4) * 32;
+    mma_ss(d_tmem, smem_desc(q_s + off, 16, 1024, kSw128), smem_desc(k_s + off, 16, 1024, kSw128),
+           idesc, ks > 0);
+  }
+  if constexpr (C::kTail != 0) {
+    const uint32_t off = C::kMainBoxes * C::kBoxBytes;
+    mma_ss(d_tmem, smem_desc(q_s + off, 16, 256, kSw32), smem_desc(k_s + off, 16, 256, kSw32),
+           idesc, 1);
+  }
+}
+
+// O[tmem] (+)= P[tmem] V[smem]; V is MN-major (d contiguous) in the same boxes.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_s,
+                                         uint32_t accumulate) {
+  using C = AttnCfg<D>;
+  constexpr uint32_t idesc_main = idesc_bf16_f32(128, C::kMainBoxes * 64, 0, 1);
+#pragma unroll
+  for (int ks = 0; ks < kBlockN / 16; ++ks) {
+    const uint32_t acc = (ks > 0) ? 1u : accumulate;
+    mma_ts(o_tmem, p_tmem + ks * 8, smem_desc(v_s + ks * 2048, C::kBoxBytes, 1024, kSw128),
+           idesc_main, acc);
+    if constexpr (C::kTail != 0) {
+      constexpr uint32_t idesc_tail = idesc_bf16_f32(128, 16, 0, 1);
+      mma_ts(o_tmem + C::kMainBoxes * 64, p_tmem + ks * 8,
+             smem_desc(v_s + C::kMainBoxes * C::kBoxBytes + ks * 512, C::kTailBytes, 256, kSw32),
+             idesc_tail, acc);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p) {
+  using C = AttnCfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q, bar_k[NS], bar_v[NS], bar_kv_empty[NS], bar_s[2],
+      bar_p[2], bar_o[2], bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work item: heavy (late, causal) pairs of every sequence first ----
+  const int lin = blockIdx.x;
+  const int h = lin % p.hq;
+  const int t = lin / p.hq;
+  const int b = t % p.batch;
+  const int pr = p.pairs_max - 1 - t / p.batch;
+  const int64_t q_start = p.cu_q[b], k_start = p.cu_k[b];
+  const int64_t q_end = p.cu_q[b + 1], k_end = p.cu_k[b + 1];
+  const int64_t Lq = q_end - q_start, Lk = k_end - k_start;
+  if (q_start < 0 || k_start < 0 || Lq < 0 || Lk < 0 || q_end > p.total_q || k_end > p.total_k ||
+      Lq > p.max_seqlen_q || Lk > p.max_seqlen_k) {
+    if (tid == 0 && pr == 0 && h == 0 && p.dev_status) atomicOr(p.dev_status, kDevBadArg);
+    return;
+  }
+  const int64_t q_lo = (int64_t)pr * 2 * kBlockM;  // first query row (within the sequence)
+  if (q_lo >= Lq) return;
+  const int g = h / (p.hq / p.hkv);
+  int64_t kv_end = Lk;
+  if (p.causal) {
+    const int64_t i_last = (q_lo + 2 * kBlockM < Lq ? q_lo + 2 * kBlockM : Lq) - 1;
+    const int64_t lim = i_last + (Lk - Lq) + 1;
+    kv_end = lim < kv_end ? lim : kv_end;
+    if (kv_end < 0) kv_end = 0;
+  }
+  const int n_tiles = (int)((kv_end + kBlockN - 1) / kBlockN);
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ[2] = {s_base, s_base + C::kTileBytes};
+  auto sK = [&](int st) { return s_base + (2 + st) * C::kTileBytes; };
+  auto sV = [&](int st) { return s_base + (2 + NS + st) * C::kTileBytes; };
+
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(smem_u32(&bar_q), 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&bar_k[i]), 1);
+      mbar_init(smem_u32(&bar_v[i]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_s[i]), 1);
+      mbar_init(smem_u32(&bar_p[i]), kBlockM);
+      mbar_init(smem_u32(&bar_o[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&maps.q);
+      prefetch_tmap(&maps.k);
+      prefetch_tmap(&maps.v);
+      const uint32_t bq = smem_u32(&bar_q);
+      if (n_tiles > 0) {
+        mbar_arrive_expect_tx(bq, 2 * C::kTileBytes);
+        for (int w = 0; w < 2; ++w)
+          load_tile<D>(sQ[w], &maps.q, &maps.q_t, bq, h, (int)(q_start + q_lo + w * kBlockM));
+      }
+      int issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % NS;
+        if (j >= NS &&
+            !mbar_wait(smem_u32(&bar_kv_empty[st]), ((j / NS) - 1) & 1, abort_flag, p.dev_status))
+          break;
+        const int tok = (int)(k_start + (int64_t)j * kBlockN);
+        mbar_arrive_expect_tx(smem_u32(&bar_k[st]), C::kTileBytes);
+        load_tile<D>(sK(st), &maps.k, &maps.k_t, smem_u32(&bar_k[st]), g, tok);
+        mbar_arrive_expect_tx(smem_u32(&bar_v[st]), C::kTileBytes);
+        load_tile<D>(sV(st), &maps.v, &maps.v_t, smem_u32(&bar_v[st]), g, tok);
+        issued = j + 1;
+      }
+      if (*abort_flag && n_tiles > 0) {
+        // Best-effort drain of copies still in flight before the CTA can exit.
+        mbar_wait(bq, 0, nullptr, nullptr);
+        for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j) {
+          mbar_wait(smem_u32(&bar_k[j % NS]), (j / NS) & 1, nullptr, nullptr);
+          mbar_wait(smem_u32(&bar_v[j % NS]), (j / NS) & 1, nullptr, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      const uint32_t S_t[2] = {tmem, tmem + 128};
+      const uint32_t O_t[2] = {tmem + 256, tmem + 384};
+      bool ok = mbar_wait(smem_u32(&bar_q), 0, abort_flag, p.dev_status) &&
+                mbar_wait(smem_u32(&bar_k[0]), 0, abort_flag, p.dev_status);
+      if (ok) {
+        tc_fence_after();
+        issue_qk<D>(S_t[0], sQ[0], sK(0));
+        mma_commit(smem_u32(&bar_s[0]));
+        issue_qk<D>(S_t[1], sQ[1], sK(0));
+        mma_commit(smem_u32(&bar_s[1]));
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        const bool more = j + 1 < n_tiles;
+        const int st1 = (j + 1) % NS;
+        const uint32_t ph1 = ((j + 1) / NS) & 1;
+        if (!mbar_wait(smem_u32(&bar_v[st]), ph, abort_flag, p.dev_status)) break;
+        // warpgroup 0
+        if (!mbar_wait(smem_u32(&bar_p[0]), j & 1, abort_flag, p.dev_status)) break;
+        tc_fence_after();
+        issue_pv<D>(O_t[0], S_t[0], sV(st), j > 0);
+        if (more) {
+          if (!mbar_wait(smem_u32(&bar_k[st1]), ph1, abort_flag, p.dev_status)) break;
+          tc_fence_after();
+          issue_qk<D>(S_t[0], sQ[0], sK(st1));
+          mma_commit(smem_u32(&bar_s[0]));
+        } else {
+          mma_commit(smem_u32(&bar_o[0]));
+        }
+        // warpgroup 1
+        if (!mbar_wait(smem_u32(&bar_p[1]), j & 1, abort_flag, p.dev_status)) break;
+        tc_fence_after();
+        issue_pv<D>(O_t[1], S_t[1], sV(st), j > 0);
+        mma_commit(smem_u32(&bar_kv_empty[st]));
+        if (more) {
+          issue_qk<D>(S_t[1], sQ[1], sK(st1));
+          mma_commit(smem_u32(&bar_s[1]));
+        } else {
+          mma_commit(smem_u32(&bar_o[1]));
+        }
+      }
+      // Drain: every MMA issued by this thread is complete before TMEM is freed.
+      mma_commit(smem_u32(&bar_drain));
+      mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int wg = (warp - 4) >> 2;         // 0 or 1
+    const int row = ((warp & 3) << 5) + lane;  // TMEM lane == row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t S_row = tmem + wg * 128 + lane_off;
+    const uint32_t O_row = tmem + 256 + wg * 128 + lane_off;
+    const int64_t i = q_lo + wg * kBlockM + row;  // query row within the sequence
+    int64_t limit = Lk;                          // keys [0, limit) visible to this row
+    if (p.causal) {
+      const int64_t lim = i + (Lk - Lq) + 1;
+      limit = lim < limit ? lim : limit;
+    }
+    const float c = p.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      // tcgen05.ld/st are warp-collective: leave the loop as a whole warp.
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_s[wg]), j & 1, abort_flag,
+                                              p.dev_status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        tmem_ld32(S_row + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
+      tmem_ld_wait();
+      float* s = reinterpret_cast<float*>(sr);
+      const int64_t kv0 = (int64_t)j * kBlockN;
+      if (kv0 + kBlockN > limit) {
+        const int64_t lim = limit - kv0;
+#pragma unroll
+        for (int cc = 0; cc < 128; ++cc)
+          if (cc >= lim) s[cc] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int cc = 1; cc < 128; ++cc) mx = fmaxf(mx, s[cc]);
+      const float m_new = fmaxf(m_ref, mx);
+      const bool resc = (m_new - m_ref) * c > 8.0f;  // false for -inf - -inf (NaN)
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2_approx((m_ref - m_new) * c);  // 0 when m_ref = -inf
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
+      float rs = 0.f;
+      // P packed as bf16 pairs into sr[0..63] (slot cc is written after s[2cc], s[2cc+1]
+      // were read, so the in-place reuse is safe).
+#pragma unroll
+      for (int cc = 0; cc < 64; ++cc) {
+        const float p0 = ex2_approx(fmaf(s[2 * cc], c, neg_mc));
+        const float p1 = ex2_approx(fmaf(s[2 * cc + 1], c, neg_mc));
+        rs += p0 + p1;
+        sr[cc] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+#pragma unroll
+      for (int q4 = 0; q4 < 2; ++q4)
+        tmem_st32(S_row + q4 * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[q4 * 32]));
+      // Rescale O (its previous PV finished: it was issued before this tile's S MMA,
+      // whose completion this thread observed).
+      if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t o[16];
+          tmem_ld16(O_row + c0, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st16(O_row + c0, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p[wg]));
+    }
+    // ---- epilogue: out = O / l, lse = m * scale + ln l ----
+    if (ok && n_tiles > 0)
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_o[wg]), 0, abort_flag, p.dev_status));
+    tc_fence_after();
+    const bool store = ok && i < Lq;
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    float* orow = p.out + ((q_start + i) * p.hq + h) * (int64_t)D;
+    if (n_tiles > 0 && ok) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t o[16];
+        tmem_ld16(O_row + c0, o);
+        tmem_ld_wait();
+        if (store) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            float4 v4 = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
+                                    __uint_as_float(o[e + 2]) * inv_l,
+                                    __uint_as_float(o[e + 3]) * inv_l);
+            *reinterpret_cast<float4*>(orow + c0 + e) = v4;
+          }
+        }
+      }
+    } else if (store) {
+      for (int c0 = 0; c0 < D; c0 += 4)
+        *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (store && p.lse != nullptr)
+      p.lse[(q_start + i) * p.hq + h] =
+          (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
+                                   int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = in[i];
+    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
+  using C = AttnCfg<D>;
+  AttnMaps maps;
+  auto make = [&](CUtensorMap* m, const void* base, int64_t tokens, int heads, uint32_t box0,
+                  CUtensorMapSwizzle sw) -> bool {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)heads, (uint64_t)tokens};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)heads * D * 2};
+    const uint32_t box[3] = {box0, 1, (uint32_t)kBlockN};
+    CUresult r = encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                                   const_cast<void*>(base), dims, strides, box, sw);
+    if (r != CUDA_SUCCESS) {
+      *drv_err = (int)r;
+      return false;
+    }
+    return true;
+  };
+  const int64_t tq = a.total_q > 0 ? a.total_q : 1, tk = a.total_k > 0 ? a.total_k : 1;
+  if (!make(&maps.q, a.q, tq, a.hq, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make(&maps.k, a.k, tk, a.hkv, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make(&maps.v, a.v, tk, a.hkv, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if constexpr (C::kTail != 0) {
+    if (!make(&maps.q_t, a.q, tq, a.hq, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make(&maps.k_t, a.k, tk, a.hkv, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make(&maps.v_t, a.v, tk, a.hkv, 16, CU_TENSOR_MAP_SWIZZLE_32B))
+      return cudaErrorInvalidValue;
+  } else {
+    maps.q_t = maps.q;
+    maps.k_t = maps.k;
+    maps.v_t = maps.v;
+  }
+  AttnParams p;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.dev_status = a.dev_status;
+  p.total_q = a.total_q;
+  p.total_k = a.total_k;
+  p.batch = a.batch;
+  p.max_seqlen_q = a.max_seqlen_q;
+  p.max_seqlen_k = a.max_seqlen_k;
+  p.hq = a.hq;
+  p.hkv = a.hkv;
+  p.causal = a.causal;
+  p.pairs_max = (a.max_seqlen_q + 2 * kBlockM - 1) / (2 * kBlockM);
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  const int64_t grid = (int64_t)a.batch * p.pairs_max * a.hq;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<D><<<(unsigned)grid, kAttnThreads, C::kSmemBytes, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return launch_d<64>(a, drv_err, stream);
+    case 80: return launch_d<80>(a, drv_err, stream);
+    case 128: return launch_d<128>(a, drv_err, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream) {
+  // n is a multiple of 4 (head_dim is), pointers 16 / 8-byte aligned.
+  const int64_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  int blocks = (int)((n4 + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  f32_to_bf16_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(in),
+                                                  reinterpret_cast<uint2*>(out), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace tts

@@ -1,0 +1,53 @@
+// Internal launch interface between the C ABI layer and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tts {
+
+// ---- top-k
+size_t topk_smem_bytes(int64_t row_stride, int k);
+cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t rows,
+                               const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                               int32_t* idx, uint32_t* dev_status, cudaStream_t stream);
+
+// ---- dense attention
+struct AttnArgs {
+  const void* q;  // bf16
+  const void* k;
+  const void* v;
+  int64_t total_q, total_k;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int batch, max_seqlen_q, max_seqlen_k, hq, hkv, d, causal;
+  float scale;
+  float* out;
+  float* lse;
+  uint32_t* dev_status;
+};
+// Returns cudaSuccess or the first error; *drv_err receives a CUresult from tensor-map encoding.
+cudaError_t launch_attn_fwd(const AttnArgs& a, int* drv_err, cudaStream_t stream);
+cudaError_t launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);
+
+// ---- sparse attention
+struct SparseArgs {
+  const void* q;         // bf16 [nq, H, dqk]
+  const void* kv_cache;  // bf16 [pages, page_size, dqk]
+  const int32_t* page_table;
+  const int32_t* idx;
+  int nq, heads, dqk, dv, num_pages, page_size, num_logical_pages, kv_len, topk;
+  float scale;
+  float* out;
+  float* lse;
+  uint32_t* dev_status;
+};
+cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t stream);
+
+// ---- tensor maps (driver entry point fetched through the runtime)
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
+                           void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                           const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+}  // namespace tts

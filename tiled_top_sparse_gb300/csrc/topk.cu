@@ -1,0 +1,217 @@
+// Deterministic top-k selection: one CTA per row.
+//
+// Definition (the stable-sort fix of "推理引擎的蝴蝶效应", section 实验方法和结果,
+// with the lower-index-wins tie rule of "AMD MI250部署DeepSeek-V4-Flash", 4.2):
+// the k window positions with the largest values, ordered by value descending
+// and, among equal values, by ascending position.
+//
+// Steps per row, all in shared memory:
+//  1. map each float of the window to an order-preserving 32-bit key
+//     (-0 folded onto +0, so equal floats get equal keys);
+//  2. MSB-first radix select over 4 x 8-bit digits finds the key T of rank k
+//     and how many elements equal to T are still needed;
+//  3. compact the selected set: every key > T, plus the lowest-position keys == T
+//     (positions ranked by a block-wide scan, so the choice never depends on
+//     thread timing);
+//  4. sort the selected (key, position) pairs as one 64-bit composite
+//     (key << 32 | ~position) descending with a bitonic network. Composites are
+//     unique, so the result is fully determined by the input.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tts {
+namespace {
+
+constexpr int kTopkThreads = 512;
+constexpr int kWarps = kTopkThreads / 32;
+
+__device__ __forceinline__ uint32_t ordered_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7FFFFFFFu) == 0) u = 0;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide exclusive scan of one int per thread; returns the exclusive prefix,
+// writes the block total to *total. Uses `warp_tot` (kWarps ints) in smem.
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = (lane < kWarps) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kWarps) warp_tot[lane] = t;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int before = (warp > 0) ? warp_tot[warp - 1] : 0;
+  *total = warp_tot[kWarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
+    const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
+    const int32_t* __restrict__ row_lens, int k, int sort_n, int32_t* __restrict__ idx,
+    uint32_t* dev_status) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint64_t* sel = reinterpret_cast<uint64_t*>(smem);                      // [sort_n]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + 8 * (size_t)sort_n);  // [row_stride]
+  __shared__ int hist[256];
+  __shared__ int warp_tot[kWarps];
+  __shared__ int s_digit, s_above, s_nsel;
+
+  const int tid = threadIdx.x;
+  const int64_t r = blockIdx.x;
+  int32_t* out = idx + r * (int64_t)k;
+  const int64_t st = row_starts[r];
+  const int64_t len = row_lens[r];
+  if (st < 0 || len < 0 || st + len > row_stride) {
+    if (tid == 0 && dev_status != nullptr) atomicOr(dev_status, kDevIndexRange);
+    for (int j = tid; j < k; j += kTopkThreads) out[j] = -1;
+    return;
+  }
+  const int n = static_cast<int>(len);
+  const float* src = logits + r * row_stride + st;
+  for (int j = tid; j < n; j += kTopkThreads) keys[j] = ordered_key(__ldg(src + j));
+  __syncthreads();
+
+  const int take = n < k ? n : k;
+  if (n > k) {
+    // ---- radix select: find the key of rank k (1-based, descending) ----
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int b = tid; b < 256; b += kTopkThreads) hist[b] = 0;
+      __syncthreads();
+      for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+        const int j = j0 + tid;
+        bool active = false;
+        uint32_t dgt = 0;
+        if (j < n) {
+          const uint32_t key = keys[j];
+          active = (key & mask) == prefix;
+          dgt = (key >> shift) & 0xFFu;
+        }
+        const uint32_t act = __ballot_sync(0xFFFFFFFFu, active);
+        if (active) {
+          const uint32_t peers = __match_any_sync(act, dgt);
+          if ((__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[dgt], __popc(peers));
+        }
+      }
+      __syncthreads();
+      if (tid < 32) {
+        // lane l owns bins 255-8l .. 248-8l (descending)
+        int c[8], s = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          c[t] = hist[255 - 8 * tid - t];
+          s += c[t];
+        }
+        int incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (tid >= o) incl += y;
+        }
+        int above = incl - s;  // count in bins strictly above this lane's first bin
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (above < remaining && remaining <= above + c[t]) {
+            s_digit = 255 - 8 * tid - t;
+            s_above = above;
+          }
+          above += c[t];
+        }
+      }
+      __syncthreads();
+      remaining -= s_above;
+      prefix |= static_cast<uint32_t>(s_digit) << shift;
+      mask |= 0xFFu << shift;
+      __syncthreads();
+    }
+    const uint32_t T = prefix;
+    const int need_ties = remaining;  // 1 <= need_ties; k - need_ties keys are > T
+    // ---- compaction: keys > T in any slot order, ties by ascending position ----
+    if (tid == 0) s_nsel = 0;
+    __syncthreads();
+    int ties_before = 0;
+    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+      const int j = j0 + tid;
+      const uint32_t key = (j < n) ? keys[j] : 0u;
+      const bool gt = (j < n) && key > T;
+      const bool eq = (j < n) && key == T;
+      int tot;
+      const int rank = ties_before + block_excl_scan(eq ? 1 : 0, warp_tot, &tot);
+      const bool pick = gt || (eq && rank < need_ties);
+      if (pick) {
+        const int slot = atomicAdd(&s_nsel, 1);
+        sel[slot] = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~j);
+      }
+      ties_before += tot;
+    }
+  } else {
+    for (int j = tid; j < n; j += kTopkThreads)
+      sel[j] = (static_cast<uint64_t>(keys[j]) << 32) | static_cast<uint32_t>(~j);
+  }
+  for (int j = take + tid; j < sort_n; j += kTopkThreads) sel[j] = 0ull;  // sorts last
+  __syncthreads();
+
+  // ---- bitonic sort, descending ----
+  for (int size = 2; size <= sort_n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < (sort_n >> 1); i += kTopkThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const uint64_t a = sel[lo], b = sel[hi];
+        if ((a < b) == desc) {
+          sel[lo] = b;
+          sel[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int j = tid; j < k; j += kTopkThreads)
+    out[j] = (j < take) ? static_cast<int32_t>(~static_cast<uint32_t>(sel[j] & 0xFFFFFFFFull)) : -1;
+}
+
+}  // namespace
+
+size_t topk_smem_bytes(int64_t row_stride, int k) {
+  const int64_t cap = row_stride < k ? row_stride : k;
+  int sort_n = 1;
+  while (sort_n < cap) sort_n <<= 1;
+  return 8 * (size_t)sort_n + 4 * (size_t)row_stride;
+}
+
+cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t rows,
+                               const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                               int32_t* idx, uint32_t* dev_status, cudaStream_t stream) {
+  const int64_t cap = row_stride < k ? row_stride : k;
+  int sort_n = 2;
+  while (sort_n < cap) sort_n <<= 1;
+  const size_t smem = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
+  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<<<rows, kTopkThreads, smem, stream>>>(logits, row_stride, row_starts,
+                                                            row_lens, k, sort_n, idx, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace tts
