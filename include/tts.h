@@ -148,7 +148,7 @@ tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows
  * page_table device int32 [num_logical_pages]
  * idx        device int32 [nq, topk]
  * out        device fp32 [nq, num_heads, dv];  lse device fp32 [nq, num_heads] or NULL
- * Built shape: num_heads = 128, dqk = 576, dv = 512, 1 <= topk <= 4096,
+ * Built shape: num_heads = 128, dqk = 576, dv = 512, 1 <= topk <= 2048,
  * page_size >= 1 (TTS_ERR_UNSUPPORTED otherwise). q and kv_cache 16-byte aligned.
  */
 tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, int32_t dqk,

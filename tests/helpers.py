@@ -40,5 +40,6 @@ def assert_lse_close(got, ref, what=""):
     r = np.asarray(ref, dtype=np.float64)
     both_inf = np.isneginf(g) & np.isneginf(r)
     assert np.array_equal(np.isneginf(g), np.isneginf(r)), f"{what}: -inf pattern differs"
-    d = np.abs(np.where(both_inf, 0.0, g - r))
+    with np.errstate(invalid="ignore"):
+        d = np.abs(np.where(both_inf, 0.0, g - r))
     assert np.all(np.isfinite(d)) and d.max(initial=0.0) <= LSE_ABS, f"{what}: lse err {d.max()}"

@@ -107,7 +107,7 @@ def test_sparse_host_validation(L):
     assert _sparse(L, ps=0) == tts.TTS_ERR_INVALID_ARG
     assert _sparse(L, scale=-1.0) == tts.TTS_ERR_INVALID_ARG
     assert _sparse(L, H=64) == tts.TTS_ERR_UNSUPPORTED
-    assert _sparse(L, topk=4097) == tts.TTS_ERR_UNSUPPORTED
+    assert _sparse(L, topk=2049) == tts.TTS_ERR_UNSUPPORTED
     assert _sparse(L, nq=0) == tts.TTS_OK
 
 

@@ -190,7 +190,7 @@ tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, i
     return TTS_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return TTS_ERR_INVALID_ARG;
   if ((int64_t)num_pages * page_size > 0x7FFFFF00LL) return TTS_ERR_UNSUPPORTED;
-  if (num_heads != 128 || dqk != 576 || dv != 512 || topk > 4096) return TTS_ERR_UNSUPPORTED;
+  if (num_heads != 128 || dqk != 576 || dv != 512 || topk > 2048) return TTS_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return TTS_ERR_INVALID_ARG;
   if (nq == 0) return TTS_OK;
   SparseArgs a;

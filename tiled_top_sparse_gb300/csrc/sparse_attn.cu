@@ -1,8 +1,436 @@
-// Paged sparse attention (placeholder until the kernel lands).
+// Sparse attention through a paged KV cache, invariant to the order of the index list.
+//
+// What it computes ("推理引擎的蝴蝶效应 -- 从V32 模型的输出不一致说起", sections
+// 实验方法和结果 and 进一步探索): for query n and head h, softmax attention over the
+// KV rows selected by idx[n, :], each fetched through the page table
+// (row = kv_cache[page_table[i / page_size], i % page_size]); K = the row's 576
+// values, V = its first 512. The write-up shows that feeding the same index set
+// in a different order changes bf16 outputs, because the online-softmax merge
+// (its equations 1-2) rounds differently per block order, and that sorting the
+// indices restores identical results. This kernel therefore sorts each query's
+// list ascending first; tiles are then visited in that canonical order with no
+// atomics, so any permutation of idx[n, :] gives bitwise identical out / lse.
+//
+// Layout of the work (one CTA = one query n and one half r of the 512 V columns):
+//   * the 128 heads form the MMA M dimension; the KV tile is 64 gathered rows;
+//   * TMEM (512 columns): Q_lo [0,128) = the 4 Q slabs (64 columns each) whose
+//     columns are also this CTA's V columns, held as the A operand of TS MMAs;
+//     S double buffer [128,192) [192,256); O half [256,512);
+//   * shared memory: the other 5 Q slabs (80 KB), and two stages of the gathered
+//     tile split into its 5 K-only slabs (40 KB) and 4 V slabs (32 KB);
+//   * warps 0-1 gather the K-only slabs, warps 2-3 the V slabs (16-byte cp.async
+//     into the 128-byte-swizzled layout the MMA reads), warp 4 issues MMAs,
+//     warps 8-11 run the softmax (one head per thread) and the epilogue.
+// Both CTAs of a query compute the same S and the same softmax bits; each
+// accumulates O for its 256 V columns (the S work is done twice so that no
+// partial scores have to be exchanged between SMs).
+#include <cstdint>
+#include <cuda_runtime.h>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace tts {
-cudaError_t launch_sparse_attn(const SparseArgs&, int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kHeads = 128;
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kTileN = 64;                  // gathered KV rows per tile
+constexpr int kSlabBytes = kTileN * 128;    // one 64-column slab of a tile: 8 KB
+constexpr int kQSlabBytes = kHeads * 128;   // one 64-column slab of Q: 16 KB
+constexpr int kKOnly = 5, kVSlabs = 4;
+constexpr int kQhiBytes = kKOnly * kQSlabBytes;      // 80 KB
+constexpr int kKStage = kKOnly * kSlabBytes;         // 40 KB
+constexpr int kVStage = kVSlabs * kSlabBytes;        // 32 KB
+constexpr int kSmemBytes = kQhiBytes + 2 * kKStage + 2 * kVStage + 1024;
+constexpr int kMaxTopk = 2048;
+constexpr int kMaxTiles = kMaxTopk / kTileN;         // 32
+
+struct SparseParams {
+  const uint16_t* q;  // bf16 bits [nq, 128, 576]
+  const uint16_t* kv;  // bf16 bits [pages * page_size, 576]
+  const int32_t* page_table;
+  const int32_t* idx;
+  float* out;
+  float* lse;
+  uint32_t* dev_status;
+  int nq, num_pages, page_size, num_logical_pages, kv_len, topk, sort_n;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ int kslab_of(int r, int i) {  // i-th K-only slab (global id)
+  return r == 0 ? 4 + i : (i < 4 ? i : 8);
 }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap qmap, const SparseParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_qhi, bar_qlo, bar_kfull[2], bar_vfull[2], bar_kempty[2],
+      bar_vempty[2], bar_s[2], bar_p[2], bar_o, bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort, s_cnt;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = blockIdx.x >> 1, r = blockIdx.x & 1;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQhi = sb;
+  const uint32_t sK0 = sb + kQhiBytes;
+  const uint32_t sV0 = sK0 + 2 * kKStage;
+  int32_t* sort_buf = reinterpret_cast<int32_t*>(smem + kQhiBytes);  // scratch before gathering
+
+  if (tid == 0) {
+    s_abort = 0;
+    s_cnt = 0;
+    mbar_init(smem_u32(&bar_qhi), 1);
+    mbar_init(smem_u32(&bar_qlo), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_kfull[i]), 64);
+      mbar_init(smem_u32(&bar_vfull[i]), 64);
+      mbar_init(smem_u32(&bar_kempty[i]), 1);
+      mbar_init(smem_u32(&bar_vempty[i]), 1);
+      mbar_init(smem_u32(&bar_s[i]), 1);
+      mbar_init(smem_u32(&bar_p[i]), 128);
+    }
+    mbar_init(smem_u32(&bar_o), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  // Q slabs that stay in shared memory: one TMA per slab, issued before the sort.
+  if (tid == 0) {
+    prefetch_tmap(&qmap);
+    mbar_arrive_expect_tx(smem_u32(&bar_qhi), kQhiBytes);
+    for (int i = 0; i < kKOnly; ++i)
+      tma_load_3d(sQhi + i * kQSlabBytes, &qmap, smem_u32(&bar_qhi), 64 * kslab_of(r, i), 0, n);
+  }
+
+  // ---- canonical order: validate, then sort the index list ascending ----
+  const int32_t* idx_row = p.idx + (int64_t)n * p.topk;
+  int my_valid = 0;
+  for (int j = tid; j < p.sort_n; j += kThreads) {
+    int key = 0x7FFFFFFF;
+    if (j < p.topk) {
+      const int32_t i = idx_row[j];
+      if (i != -1) {
+        bool ok = i >= 0 && i < p.kv_len && (i / p.page_size) < p.num_logical_pages;
+        if (ok) {
+          const int32_t pg = p.page_table[i / p.page_size];
+          ok = pg >= 0 && pg < p.num_pages;
+        }
+        if (ok) {
+          key = i;
+          ++my_valid;
+        } else if (p.dev_status != nullptr) {
+          atomicOr(p.dev_status, kDevIndexRange);
+        }
+      }
+    }
+    sort_buf[j] = key;
+  }
+  if (my_valid) atomicAdd(&s_cnt, my_valid);
+  __syncthreads();
+  for (int size = 2; size <= p.sort_n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < (p.sort_n >> 1); i += kThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const int a = sort_buf[lo], b = sort_buf[hi];
+        if ((a > b) == asc) {
+          sort_buf[lo] = b;
+          sort_buf[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  const int cnt = s_cnt;
+  const int n_tiles = (cnt + kTileN - 1) / kTileN;
+  // Producer threads keep the physical row of their entry of every tile.
+  int32_t my_row[kMaxTiles];
+  if (warp < 4) {
+    const int e = tid & 63;
+#pragma unroll
+    for (int j = 0; j < kMaxTiles; ++j) {
+      const int pos = j * kTileN + e;
+      int32_t row = -1;
+      if (pos < cnt) {
+        const int32_t i = sort_buf[pos];
+        row = p.page_table[i / p.page_size] * p.page_size + i % p.page_size;
+      }
+      my_row[j] = row;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // sort scratch is free from here on
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ Q_lo -> TMEM, gather
+    {
+      const int h = tid;  // warp w covers TMEM lanes 32w..32w+31
+      const uint32_t* qrow =
+          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)n * kHeads + h) * kDqk);
+      for (int i = 0; i < kVSlabs; ++i) {
+        uint32_t v[32];
+        const uint4* src = reinterpret_cast<const uint4*>(qrow + (4 * r + i) * 32);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = __ldg(src + c);
+          v[4 * c] = x.x;
+          v[4 * c + 1] = x.y;
+          v[4 * c + 2] = x.z;
+          v[4 * c + 3] = x.w;
+        }
+        tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + i * 32, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_qlo));
+    }
+    const bool kside = warp < 2;
+    const int e = tid & 63;
+    const int nslab = kside ? kKOnly : kVSlabs;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      if (j >= 2) {
+        const uint32_t eb = smem_u32(kside ? &bar_kempty[st] : &bar_vempty[st]);
+        if (!mbar_wait(eb, ((j >> 1) - 1) & 1, abort_flag, p.dev_status)) break;
+      }
+      const int32_t row = my_row[j];
+      const uint16_t* src_row = p.kv + (int64_t)(row < 0 ? 0 : row) * kDqk;
+      const uint32_t src_bytes = row < 0 ? 0u : 16u;
+      const uint32_t dst_base = (kside ? sK0 + st * kKStage : sV0 + st * kVStage) + e * 128;
+      for (int i = 0; i < nslab; ++i) {
+        const int g = kside ? kslab_of(r, i) : 4 * r + i;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          cp_async_16(dst_base + i * kSlabBytes + ((c ^ (e & 7)) << 4), src_row + g * 64 + c * 8,
+                      src_bytes);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(kside ? &bar_kfull[st] : &bar_vfull[st]));
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTileN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, 0, 1);
+      const uint32_t S_t[2] = {tmem + 128, tmem + 192};
+      const uint32_t O_t = tmem + 256;
+      const uint64_t dq = smem_desc(sQhi, 16, 1024, kSw128);
+      const uint64_t dk[2] = {smem_desc(sK0, 16, 1024, kSw128),
+                              smem_desc(sK0 + kKStage, 16, 1024, kSw128)};
+      const uint64_t dvk[2] = {smem_desc(sV0, 16, 1024, kSw128),
+                               smem_desc(sV0 + kVStage, 16, 1024, kSw128)};
+      const uint64_t dvn[2] = {smem_desc(sV0, kSlabBytes, 1024, kSw128),
+                               smem_desc(sV0 + kVStage, kSlabBytes, 1024, kSw128)};
+      bool ok = mbar_wait(smem_u32(&bar_qhi), 0, abort_flag, p.dev_status) &&
+                mbar_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status);
+      // S(t) = Q K^T for tile t into S buffer t&1: K-only slabs (Q from smem), then
+      // V slabs (Q from TMEM). The order of the 36 partial products is fixed.
+      auto issue_s = [&](int t) -> bool {
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (!mbar_wait(smem_u32(&bar_kfull[st]), ph, abort_flag, p.dev_status)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < kKOnly; ++i)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(S_t[st], dq + ((i * kQSlabBytes + ks * 32) >> 4),
+                   dk[st] + ((i * kSlabBytes + ks * 32) >> 4), idesc_s, (i | ks) != 0);
+        mma_commit(smem_u32(&bar_kempty[st]));
+        if (!mbar_wait(smem_u32(&bar_vfull[st]), ph, abort_flag, p.dev_status)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < kVSlabs; ++i)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts(S_t[st], tmem + i * 32 + ks * 8, dvk[st] + ((i * kSlabBytes + ks * 32) >> 4),
+                   idesc_s, 1);
+        mma_commit(smem_u32(&bar_s[st]));
+        return true;
+      };
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0) && (n_tiles < 2 || issue_s(1));
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(smem_u32(&bar_p[st]), (j >> 1) & 1, abort_flag, p.dev_status)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTileN / 16; ++ks)
+          mma_ts(O_t, S_t[st] + ks * 8, dvn[st] + ((ks * 2048) >> 4), idesc_pv,
+                 (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bar_vempty[st]));
+        if (j + 1 == n_tiles) mma_commit(smem_u32(&bar_o));
+        if (j + 2 < n_tiles && !issue_s(j + 2)) break;
+      }
+      mma_commit(smem_u32(&bar_drain));
+      mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int h = ((warp & 3) << 5) + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c = p.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      const uint32_t S_row = tmem + 128 + st * 64 + lane_off;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_s[st]), (j >> 1) & 1, abort_flag,
+                                              p.dev_status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld32(S_row, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(S_row + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait();
+      float* s = reinterpret_cast<float*>(sr);
+      const int valid = cnt - j * kTileN;  // entries of this tile that exist
+      if (valid < kTileN) {
+#pragma unroll
+        for (int cc = 0; cc < kTileN; ++cc)
+          if (cc >= valid) s[cc] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int cc = 1; cc < kTileN; ++cc) mx = fmaxf(mx, s[cc]);
+      const float m_new = fmaxf(m_ref, mx);
+      const bool resc = (m_new - m_ref) * c > 8.0f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2_approx((m_ref - m_new) * c);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
+      float rs = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < kTileN / 2; ++cc) {
+        const float p0 = ex2_approx(fmaf(s[2 * cc], c, neg_mc));
+        const float p1 = ex2_approx(fmaf(s[2 * cc + 1], c, neg_mc));
+        rs += p0 + p1;
+        sr[cc] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+      tmem_st32(S_row, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+      if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+        // O must hold every PV up to tile j-1: PV(j-1) is the last one issued.
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_vempty[(j - 1) & 1]),
+                                                ((j - 1) >> 1) & 1, abort_flag, p.dev_status));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t O_row = tmem + 256 + lane_off;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(O_row + c0, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(O_row + c0, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p[st]));
+    }
+    // ---- epilogue ----
+    if (ok && n_tiles > 0)
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_o), 0, abort_flag, p.dev_status));
+    tc_fence_after();
+    float* orow = p.out + ((int64_t)n * kHeads + h) * kDv + 256 * r;
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    if (ok && n_tiles > 0) {
+      const uint32_t O_row = tmem + 256 + lane_off;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(O_row + c0, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(orow + c0 + e) =
+              make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
+                          __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+      }
+    } else if (ok) {
+      for (int c0 = 0; c0 < 256; c0 += 4)
+        *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (ok && r == 0 && p.lse != nullptr)
+      p.lse[(int64_t)n * kHeads + h] =
+          (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
+  }
+
+  // The Q_hi copy must have landed before the CTA may exit (it is otherwise only
+  // waited for by the MMA thread, which skips its work when no entry is valid).
+  if (tid == 0) mbar_wait(smem_u32(&bar_qhi), 0, nullptr, p.dev_status);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t stream) {
+  if (a.heads != kHeads || a.dqk != kDqk || a.dv != kDv || a.topk > kMaxTopk)
+    return cudaErrorNotSupported;
+  CUtensorMap qmap;
+  const uint64_t dims[3] = {(uint64_t)kDqk, (uint64_t)kHeads, (uint64_t)a.nq};
+  const uint64_t strides[2] = {(uint64_t)kDqk * 2, (uint64_t)kHeads * kDqk * 2};
+  const uint32_t box[3] = {64, kHeads, 1};
+  CUresult rr = encode_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                                  const_cast<void*>(a.q), dims, strides, box,
+                                  CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rr != CUDA_SUCCESS) {
+    *drv_err = (int)rr;
+    return cudaErrorInvalidValue;
+  }
+  SparseParams p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.kv = static_cast<const uint16_t*>(a.kv_cache);
+  p.page_table = a.page_table;
+  p.idx = a.idx;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.dev_status = a.dev_status;
+  p.nq = a.nq;
+  p.num_pages = a.num_pages;
+  p.page_size = a.page_size;
+  p.num_logical_pages = a.num_logical_pages;
+  p.kv_len = a.kv_len;
+  p.topk = a.topk;
+  int sort_n = 64;
+  while (sort_n < a.topk) sort_n <<= 1;
+  p.sort_n = sort_n;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  sparse_attn_kernel<<<2 * a.nq, kThreads, kSmemBytes, stream>>>(qmap, p);
+  return cudaGetLastError();
+}
+
 }  // namespace tts
