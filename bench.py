@@ -1,0 +1,512 @@
+#!/usr/bin/env python3
+"""Benchmark of the tiled / top-k / sparse attention hot path on GB300.
+
+One step = one pass of the whole hot path over synthetic inputs shaped like the
+pages' workloads, every part through the C ABI of libtts.so:
+  vision  dense attention, N = 8547, 16 heads, d = 80, non-causal      (tensor cores)
+  varlen  causal GQA prefill, 8 sequences <= 32768 tokens, 32/8 heads, d = 128
+  topk    top-2048 of (323, 2590) indexer logits                        (HBM)
+  sparse  323 queries x 128 heads, 576/512, 2048 paged indices          (gather)
+
+Prints one JSON line (rank 0). `value` = attention TFLOP/s of the whole step
+(dense + sparse FLOPs / step time); per-part figures are under `components`.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+`--impl reference` times the float64 CPU oracle (the only reference there is:
+the pages ship no code) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "attn TFLOP/s & % bf16 peak; top-k rows/s & sparse-attn GB/s vs HBM roofline"
+WORKLOAD = "hot-path step: vision attn (8547 tok, 16h, d80) + varlen causal GQA prefill " \
+           "(8 seqs <= 32768 tok, 32/8h, d128) + top-k (323x2590, k 2048) + sparse MLA attn " \
+           "(323 q x 128h, 576/512, 2048 paged idx)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS = {"vision": "attn_fwd_kernel<80>", "varlen": "attn_fwd_kernel<128>",
+           "topk": "topk_select_kernel", "sparse": "sparse_attn_kernel"}
+KERNEL_SOURCES = {"vision": "attn_fwd.cu", "varlen": "attn_fwd.cu", "topk": "topk.cu",
+                  "sparse": "sparse_attn.cu"}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(part: str) -> str:
+    h = hashlib.sha256()
+    for fn in (KERNEL_SOURCES[part], "ptx.cuh"):
+        with open(os.path.join(ROOT, "tiled_top_sparse_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(part: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(part)
+    if not e or e.get("source_hash") != source_hash(part):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a host float over all ranks (the step time that bounds the job)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- workload
+class Step:
+    """Device-resident inputs/outputs of one hot-path step and the four calls."""
+
+    def __init__(self, dev, small=False):
+        import tiled_top_sparse_gb300 as tts
+        self.tts = tts
+        self.dev = dev
+        self.vis = W.vision()
+        # small: a profiling-sized varlen batch (still larger than L2 in total)
+        self.var = W.varlen(lengths=[4096, 3000, 2000, 1000]) if small else W.varlen()
+        self.tk = W.topk_inputs()
+        self.sp = W.sparse_inputs()
+        g = lambda t: t.to(dev)  # noqa: E731
+        self.d_vis = [g(self.vis.q), g(self.vis.k), g(self.vis.v), g(self.vis.cu_seqlens_q),
+                      g(self.vis.cu_seqlens_k)]
+        self.d_var = [g(self.var.q), g(self.var.k), g(self.var.v), g(self.var.cu_seqlens_q),
+                      g(self.var.cu_seqlens_k)]
+        self.d_tk = [g(self.tk.logits), g(self.tk.row_starts), g(self.tk.row_lens)]
+        self.d_sp = [g(self.sp.q), g(self.sp.kv_cache), g(self.sp.page_table), g(self.sp.idx)]
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.o_vis = torch.empty(self.vis.q.shape, **f32)
+        self.l_vis = torch.empty(self.vis.q.shape[:2], **f32)
+        self.o_var = torch.empty(self.var.q.shape, **f32)
+        self.l_var = torch.empty(self.var.q.shape[:2], **f32)
+        self.o_idx = torch.empty((self.tk.logits.shape[0], self.tk.k), dtype=torch.int32,
+                                 device=dev)
+        self.o_sp = torch.empty((self.sp.q.shape[0], self.sp.q.shape[1], self.sp.dv), **f32)
+        self.l_sp = torch.empty(self.sp.q.shape[:2], **f32)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.flops = {"vision": self.vis.flops(), "varlen": self.var.flops(),
+                      "sparse": self.sp.flops()}
+        self.topk_bytes = self.tk.bytes()
+        self.gathered = self.sp.gathered_bytes()
+
+    def inputs(self):
+        return self.d_vis[:3] + self.d_var[:3] + self.d_tk[:1] + self.d_sp[:2] + self.d_sp[3:]
+
+    def outputs(self):
+        return [self.o_vis, self.l_vis, self.o_var, self.l_var, self.o_idx, self.o_sp, self.l_sp]
+
+    def part(self, name):
+        t = self.tts
+        if name == "vision":
+            q, k, v, cq, ck = self.d_vis
+            t.attn_fwd_varlen(q, k, v, cq, ck, self.vis.max_seqlen_q, self.vis.max_seqlen_k,
+                              False, self.vis.scale, out=self.o_vis, lse=self.l_vis,
+                              status=self.status)
+        elif name == "varlen":
+            q, k, v, cq, ck = self.d_var
+            t.attn_fwd_varlen(q, k, v, cq, ck, self.var.max_seqlen_q, self.var.max_seqlen_k,
+                              True, self.var.scale, out=self.o_var, lse=self.l_var,
+                              status=self.status)
+        elif name == "topk":
+            lg, rs, rl = self.d_tk
+            t.topk_select(lg, rs, rl, self.tk.k, idx=self.o_idx, status=self.status)
+        elif name == "sparse":
+            q, kv, pt, ix = self.d_sp
+            t.sparse_attn_paged(q, kv, pt, ix, self.sp.kv_len, self.sp.scale, dv=self.sp.dv,
+                                out=self.o_sp, lse=self.l_sp, status=self.status)
+
+    PARTS = ("vision", "varlen", "topk", "sparse")
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(n_rows: int = 192, n_queries: int = 8):
+    """Time the float64 oracle on bounded samples of each part.
+
+    Returns {part: (work, seconds, description)}; work is FLOPs for the attention
+    parts and rows for top-k.
+    """
+    import oracle
+    oracle.build()
+    vis, var, tk, sp = _inputs_cpu()
+    g = np.random.default_rng(7)
+    res = {}
+    n = max(1, int(n_rows))
+    tok = g.integers(0, 8547, n).astype(np.int32)
+    head = g.integers(0, 16, n).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attn_varlen(*vis["qkv"], vis["cq"], vis["ck"], False, vis["scale"], rows=(tok, head))
+    res["vision"] = (n * 8547 * 80 * 4.0, time.perf_counter() - t0, f"{n} sampled rows")
+    cq = var["cq"]
+    T = int(cq[-1])
+    tok = g.integers(0, T, n).astype(np.int32)
+    head = g.integers(0, 32, n).astype(np.int32)
+    b = np.searchsorted(cq, tok, side="right") - 1
+    vis_keys = (tok - cq[b] + 1).astype(np.float64)  # causal, Lq == Lk
+    t0 = time.perf_counter()
+    oracle.attn_varlen(*var["qkv"], cq, var["ck"], True, var["scale"], rows=(tok, head))
+    res["varlen"] = (float(vis_keys.sum()) * 128 * 4.0, time.perf_counter() - t0,
+                     f"{n} sampled rows")
+    t0 = time.perf_counter()
+    oracle.topk(tk.logits.numpy(), tk.row_starts.numpy(), tk.row_lens.numpy(), tk.k)
+    res["topk"] = (float(tk.logits.shape[0]), time.perf_counter() - t0, "all 323 rows")
+    nq = max(1, int(n_queries))
+    rows = g.choice(sp.q.shape[0], nq, replace=False)
+    t0 = time.perf_counter()
+    oracle.sparse_paged(sp.q.float().numpy()[rows], sp.kv_cache.float().numpy(),
+                        sp.page_table.numpy(), sp.idx.numpy()[rows], sp.kv_len, sp.dv, sp.scale)
+    valid = int((sp.idx[rows] >= 0).sum())
+    res["sparse"] = (2.0 * 128 * valid * (576 + 512), time.perf_counter() - t0,
+                     f"{nq} sampled queries")
+    return res
+
+
+_CPU_INPUTS = None
+
+
+def _inputs_cpu():
+    global _CPU_INPUTS
+    if _CPU_INPUTS is None:
+        vis, var, tk, sp = W.vision(), W.varlen(), W.topk_inputs(), W.sparse_inputs()
+        pack = lambda d: {"qkv": [t.float().numpy() for t in (d.q, d.k, d.v)],  # noqa: E731
+                          "cq": d.cu_seqlens_q.numpy(), "ck": d.cu_seqlens_k.numpy(),
+                          "scale": d.scale}
+        _CPU_INPUTS = (pack(vis), pack(var), tk, sp)
+    return _CPU_INPUTS
+
+
+def sized_sample(target_s: float):
+    """Pick sample sizes so one oracle sample takes about target_s seconds."""
+    probe = oracle_sample(16, 1)
+    per_row = (probe["vision"][1] + probe["varlen"][1]) / 16
+    per_q = probe["sparse"][1]
+    fixed = probe["topk"][1]
+    budget = max(0.05, target_s - fixed)
+    # split the budget: half on dense rows, half on sparse queries
+    n_rows = int(min(4096, max(1, 0.5 * budget / max(per_row, 1e-6))))
+    n_q = int(min(323, max(1, 0.5 * budget / max(per_q, 1e-6))))
+    return n_rows, n_q
+
+
+def cpu_cores_used():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
+
+
+def cpu_baseline_entry(res):
+    attn_flops = res["vision"][0] + res["varlen"][0] + res["sparse"][0]
+    attn_time = res["vision"][1] + res["varlen"][1] + res["sparse"][1]
+    return {"value": attn_flops / attn_time / 1e12, "unit": "TFLOP/s", "cores": cpu_cores_used(),
+            "kind": "oracle",
+            "sample": "float64 oracle on bounded samples: vision %s, varlen %s, sparse %s; "
+                      "top-k %s (%.1f rows/s)" % (res["vision"][2], res["varlen"][2],
+                                                  res["sparse"][2], res["topk"][2],
+                                                  res["topk"][0] / res["topk"][1])}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    # Each step is a bounded sample so that warm-up + timed steps end within ~2 minutes.
+    per_step = max(0.1, min(10.0, 100.0 / max(1, args.steps + args.warmup)))
+    n_rows, n_q = sized_sample(per_step)
+    steps = []
+    res = None
+    for _ in range(args.warmup):
+        oracle_sample(n_rows, n_q)
+    for _ in range(args.steps):
+        res = oracle_sample(n_rows, n_q)
+        steps.append(res)
+    flops = sum(r["vision"][0] + r["varlen"][0] + r["sparse"][0] for r in steps)
+    secs = sum(r["vision"][1] + r["varlen"][1] + r["sparse"][1] + r["topk"][1] for r in steps)
+    value = flops / secs / 1e12
+    cb = cpu_baseline_entry(res)
+    cb["value"] = value
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import tiled_top_sparse_gb300 as tts
+    tts.lib()
+    step = Step(dev, small=args.small)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    parts = tuple(p for p in Step.PARTS if p in args.parts.split(","))
+
+    def one_step(ev=None):
+        for i, p in enumerate(parts):
+            if ev is not None:
+                ev[i].record(stream)
+            step.part(p)
+        if ev is not None:
+            ev[len(parts)].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    tts.check_status(step.status, "bench warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        time.sleep(0.25)  # let the sampler start
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps (outside the step's events)
+            one_step(evs[k])
+        torch.cuda.synchronize()
+        t_wall1 = time.perf_counter()
+        barrier(world)
+    tts.check_status(step.status, "bench timed region")
+    per_part = {p: [] for p in parts}
+    step_ms = []
+    for k in range(args.steps):
+        e = evs[k]
+        for i, p in enumerate(parts):
+            per_part[p].append(e[i].elapsed_time(e[i + 1]))
+        step_ms.append(e[0].elapsed_time(e[len(parts)]))
+    ms_step_local = float(np.mean(step_ms))
+    ms_step = max_over_ranks(ms_step_local, world)
+    attn_flops = sum(step.flops[p] for p in parts if p in step.flops)
+    value = world * attn_flops / (ms_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    timed_s = t_wall1 - t_wall0
+    tensor_peak = peaks["bf16_tflops_sustained"] if timed_s > 1.0 else peaks["bf16_tflops"]
+    tensor_peak_name = "bf16_tflops_sustained" if timed_s > 1.0 else "bf16_tflops"
+    comp = {}
+    for p in parts:
+        ms = float(np.mean(per_part[p]))
+        c = {"ms": ms, "kernel": KERNELS[p], "launches_per_step": 1}
+        if p in ("vision", "varlen"):
+            tf = step.flops[p] / (ms * 1e-3) / 1e12
+            c.update({"tflops": tf, "frac_bf16_peak": tf / tensor_peak})
+        elif p == "topk":
+            gbs = step.topk_bytes / (ms * 1e-3) / 1e9
+            c.update({"rows_per_s": step.tk.logits.shape[0] / (ms * 1e-3), "gbs": gbs,
+                      "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": step.topk_bytes})
+        else:
+            gbs = step.gathered / (ms * 1e-3) / 1e9
+            tf = step.flops[p] / (ms * 1e-3) / 1e12
+            c.update({"gathered_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+                      "gathered_bytes": step.gathered, "tflops": tf,
+                      "frac_bf16_peak": tf / tensor_peak})
+        comp[p] = c
+    dom = max(parts, key=lambda p: comp[p]["ms"])
+    dc = comp[dom]
+    if dom in ("vision", "varlen"):
+        roof = {"bound": "tensor", "achieved": dc["tflops"], "peak": tensor_peak,
+                "unit": "TFLOP/s", "frac": dc["tflops"] / tensor_peak}
+    elif dom == "topk":
+        roof = {"bound": "hbm", "achieved": dc["gbs"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": dc["frac_hbm"]}
+    else:
+        roof = {"bound": "tensor", "achieved": dc["tflops"], "peak": tensor_peak,
+                "unit": "TFLOP/s", "frac": dc["tflops"] / tensor_peak}
+    roof["kernel"] = dc["kernel"]
+    roof["traffic"] = profiled_traffic(dom)
+    roof["peak_source"] = f"{peak_src} ({'hbm_gbs' if roof['unit'] == 'GB/s' else tensor_peak_name})"
+
+    # ---- end to end through the public API: pinned host inputs in, results out ----
+    e2e = None
+    if rank == 0 or world > 1:
+        ins = step.inputs()
+        outs = step.outputs()
+        h_in = [t.cpu().pin_memory() for t in ins]
+        h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        n_e2e = max(1, min(args.steps, 10))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(n_e2e):
+            flush.zero_()
+            e0.record(stream)
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            one_step()
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms_e2e = max_over_ranks(float(np.mean(times)), world)
+        e2e = {"value": world * attn_flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins)),
+               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs))}
+        tts.check_status(step.status, "bench e2e")
+
+    if rank != 0:
+        return
+    cpu_base = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu_base = cpu_baseline_entry(oracle_sample(*sized_sample(15.0)))
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1
+                   else "single GPU", "lengths_varlen": step.var.lengths_q,
+                   "l2": "flushed between steps (256 MB write outside the step's events); "
+                         "step inputs also exceed L2",
+                   "ms_wall_timed_region": (t_wall1 - t_wall0) * 1e3},
+        "components": comp, "roofline": roof, "cpu_baseline": cpu_base, "e2e": e2e,
+        "gpu_launches": len(parts) * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--parts", default="vision,varlen,topk,sparse",
+                    help="subset of the step to run (profiling); default: the whole hot path")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling-sized varlen batch (4 sequences, 10096 tokens)")
+    args = ap.parse_args()
+    rank, world, local = dist_init(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
