@@ -158,6 +158,43 @@ tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, i
                                  int32_t topk, float scale, float* out, float* lse,
                                  uint32_t* dev_status, void* stream);
 
+/*
+ * Allocation-free variant of tts_attn_fwd_varlen for fp32 q / k / v.
+ *
+ * This entry point has no counterpart in the pages; it exists for callers that
+ * cannot allocate device memory when they call: for example code running while
+ * another runtime has reserved the device's whole memory pool, or a serving loop
+ * that forbids allocation after start-up. The fp32 path needs scratch for the bf16
+ * copies of its inputs; here that scratch is a fixed array inside the library
+ * (TTS_NOALLOC_SCRATCH_BYTES of device memory, reserved on every GPU that loads the
+ * library until the process exits), so the call takes no workspace argument and
+ * calls no allocator. Everything else -- arguments, layouts, results, errors -- is
+ * as for tts_attn_fwd_varlen with in_dtype = TTS_F32.
+ *
+ * - Inputs whose bf16 copies need more than TTS_NOALLOC_SCRATCH_BYTES, i.e.
+ *   2 * (total_q * num_heads_q + 2 * total_k * num_heads_kv) * head_dim bytes
+ *   (each part rounded up to 256), are rejected with TTS_ERR_WORKSPACE before any
+ *   work is enqueued.
+ * - The first call on a device looks up the array's device address on that device
+ *   (which must be current) and caches it; make that first call before capturing
+ *   a stream into a CUDA graph.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   contents; nothing in it needs to start at zero, because each call overwrites
+ *   every byte it reads. Calls that overlap on the GPU (e.g. on two streams at
+ *   once) race on the array and give undefined results: serialise them.
+ */
+#define TTS_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+tts_status tts_attn_fwd_varlen_f32_noalloc(const float* q, const float* k, const float* v,
+                                           int64_t total_q, int64_t total_k,
+                                           const int32_t* cu_seqlens_q,
+                                           const int32_t* cu_seqlens_k, int32_t batch,
+                                           int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                           int32_t num_heads_q, int32_t num_heads_kv,
+                                           int32_t head_dim, int32_t causal, float scale,
+                                           float* out, float* lse, uint32_t* dev_status,
+                                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -45,6 +45,7 @@ EXPORTED = (
     "tts_attn_fwd_varlen",
     "tts_topk_select",
     "tts_sparse_attn_paged",
+    "tts_attn_fwd_varlen_f32_noalloc",
 )
 
 
@@ -82,6 +83,9 @@ def lib() -> ctypes.CDLL:
     L.tts_sparse_attn_paged.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, i32, i32, P, i32,
                                         f32, P, P, P, P]
     L.tts_sparse_attn_paged.restype = ctypes.c_int
+    L.tts_attn_fwd_varlen_f32_noalloc.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, i32,
+                                                  i32, i32, i32, f32, P, P, P, P]
+    L.tts_attn_fwd_varlen_f32_noalloc.restype = ctypes.c_int
     _lib = L
     return L
 
