@@ -79,39 +79,35 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* main,
     tma_load_3d(dst + C::kMainBoxes * C::kBoxBytes, tail, bar, C::kMainBoxes * 64, head, token);
 }
 
-// S[tmem] = Q[smem] K[smem]^T over the D-deep contraction.
+// S[tmem] = Q[smem] K[smem]^T over the D-deep contraction. q_d / k_d are the
+// descriptors of the tiles' first box; every other K step is a constant offset
+// (the 14-bit start-address field never carries: shared addresses are < 256 KB).
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_s, uint32_t k_s) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_d, uint64_t k_d,
+                                         uint64_t q_tail_d, uint64_t k_tail_d) {
   using C = AttnCfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(128, kBlockN, 0, 0);
 #pragma unroll
   for (int ks = 0; ks < C::kMainBoxes * 4; ++ks) {
-    const uint32_t off = (ks / 4) * C::kBoxBytes + (ks % 4) * 32;
-    mma_ss(d_tmem, smem_desc(q_s + off, 16, 1024, kSw128), smem_desc(k_s + off, 16, 1024, kSw128),
-           idesc, ks > 0);
+    const uint32_t off = ((ks / 4) * C::kBoxBytes + (ks % 4) * 32) >> 4;
+    mma_ss(d_tmem, q_d + off, k_d + off, idesc, ks > 0);
   }
-  if constexpr (C::kTail != 0) {
-    const uint32_t off = C::kMainBoxes * C::kBoxBytes;
-    mma_ss(d_tmem, smem_desc(q_s + off, 16, 256, kSw32), smem_desc(k_s + off, 16, 256, kSw32),
-           idesc, 1);
-  }
+  if constexpr (C::kTail != 0) mma_ss(d_tmem, q_tail_d, k_tail_d, idesc, 1);
 }
 
 // O[tmem] (+)= P[tmem] V[smem]; V is MN-major (d contiguous) in the same boxes.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_s,
-                                         uint32_t accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_d,
+                                         uint64_t v_tail_d, uint32_t accumulate) {
   using C = AttnCfg<D>;
   constexpr uint32_t idesc_main = idesc_bf16_f32(128, C::kMainBoxes * 64, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < kBlockN / 16; ++ks) {
     const uint32_t acc = (ks > 0) ? 1u : accumulate;
-    mma_ts(o_tmem, p_tmem + ks * 8, smem_desc(v_s + ks * 2048, C::kBoxBytes, 1024, kSw128),
-           idesc_main, acc);
+    mma_ts(o_tmem, p_tmem + ks * 8, v_d + ((ks * 2048) >> 4), idesc_main, acc);
     if constexpr (C::kTail != 0) {
       constexpr uint32_t idesc_tail = idesc_bf16_f32(128, 16, 0, 1);
-      mma_ts(o_tmem + C::kMainBoxes * 64, p_tmem + ks * 8,
-             smem_desc(v_s + C::kMainBoxes * C::kBoxBytes + ks * 512, C::kTailBytes, 256, kSw32),
+      mma_ts(o_tmem + C::kMainBoxes * 64, p_tmem + ks * 8, v_tail_d + ((ks * 512) >> 4),
              idesc_tail, acc);
     }
   }
@@ -228,13 +224,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       const uint32_t S_t[2] = {tmem, tmem + 128};
       const uint32_t O_t[2] = {tmem + 256, tmem + 384};
+      constexpr uint32_t kTailOff = C::kMainBoxes * C::kBoxBytes;
+      uint64_t qd[2], qtd[2], kd[NS], ktd[NS], vd[NS], vtd[NS];
+      for (int w = 0; w < 2; ++w) {
+        qd[w] = smem_desc(sQ[w], 16, 1024, kSw128);
+        qtd[w] = smem_desc(sQ[w] + kTailOff, 16, 256, kSw32);
+      }
+      for (int i = 0; i < NS; ++i) {
+        kd[i] = smem_desc(sK(i), 16, 1024, kSw128);
+        ktd[i] = smem_desc(sK(i) + kTailOff, 16, 256, kSw32);
+        vd[i] = smem_desc(sV(i), C::kBoxBytes, 1024, kSw128);
+        vtd[i] = smem_desc(sV(i) + kTailOff, C::kTailBytes, 256, kSw32);
+      }
       bool ok = mbar_wait(smem_u32(&bar_q), 0, abort_flag, p.dev_status) &&
                 mbar_wait(smem_u32(&bar_k[0]), 0, abort_flag, p.dev_status);
       if (ok) {
         tc_fence_after();
-        issue_qk<D>(S_t[0], sQ[0], sK(0));
+        issue_qk<D>(S_t[0], qd[0], kd[0], qtd[0], ktd[0]);
         mma_commit(smem_u32(&bar_s[0]));
-        issue_qk<D>(S_t[1], sQ[1], sK(0));
+        issue_qk<D>(S_t[1], qd[1], kd[0], qtd[1], ktd[0]);
         mma_commit(smem_u32(&bar_s[1]));
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
@@ -247,11 +255,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // warpgroup 0
         if (!mbar_wait(smem_u32(&bar_p[0]), j & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
-        issue_pv<D>(O_t[0], S_t[0], sV(st), j > 0);
+        issue_pv<D>(O_t[0], S_t[0], vd[st], vtd[st], j > 0);
         if (more) {
           if (!mbar_wait(smem_u32(&bar_k[st1]), ph1, abort_flag, p.dev_status)) break;
           tc_fence_after();
-          issue_qk<D>(S_t[0], sQ[0], sK(st1));
+          issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1]);
           mma_commit(smem_u32(&bar_s[0]));
         } else {
           mma_commit(smem_u32(&bar_o[0]));
@@ -259,10 +267,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // warpgroup 1
         if (!mbar_wait(smem_u32(&bar_p[1]), j & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
-        issue_pv<D>(O_t[1], S_t[1], sV(st), j > 0);
+        issue_pv<D>(O_t[1], S_t[1], vd[st], vtd[st], j > 0);
         mma_commit(smem_u32(&bar_kv_empty[st]));
         if (more) {
-          issue_qk<D>(S_t[1], sQ[1], sK(st1));
+          issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1]);
           mma_commit(smem_u32(&bar_s[1]));
         } else {
           mma_commit(smem_u32(&bar_o[1]));
@@ -307,10 +315,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int cc = 0; cc < 128; ++cc)
           if (cc >= lim) s[cc] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int cc = 1; cc < 128; ++cc) mx = fmaxf(mx, s[cc]);
-      const float m_new = fmaxf(m_ref, mx);
+      const float m_new = fmaxf(m_ref, row_max<128>(s));
       const bool resc = (m_new - m_ref) * c > 8.0f;  // false for -inf - -inf (NaN)
       float alpha = 1.f;
       if (resc) {
@@ -319,17 +324,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_ref = m_new;
       }
       const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
-      float rs = 0.f;
       // P packed as bf16 pairs into sr[0..63] (slot cc is written after s[2cc], s[2cc+1]
-      // were read, so the in-place reuse is safe).
+      // were read, so the in-place reuse is safe). Two partial row sums, added at the end.
+      float2 rs2 = make_float2(0.f, 0.f);
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_mc, neg_mc);
 #pragma unroll
       for (int cc = 0; cc < 64; ++cc) {
-        const float p0 = ex2_approx(fmaf(s[2 * cc], c, neg_mc));
-        const float p1 = ex2_approx(fmaf(s[2 * cc + 1], c, neg_mc));
-        rs += p0 + p1;
-        sr[cc] = pack_bf16x2(p0, p1);
+        float2 x = ffma2(make_float2(s[2 * cc], s[2 * cc + 1]), c2, nm2);
+        x.x = ex2_approx(x.x);
+        x.y = ex2_approx(x.y);
+        rs2 = fadd2(rs2, x);
+        sr[cc] = pack_bf16x2(x.x, x.y);
       }
-      l += rs;
+      l += rs2.x + rs2.y;
 #pragma unroll
       for (int q4 = 0; q4 < 2; ++q4)
         tmem_st32(S_row + q4 * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[q4 * 32]));

@@ -33,7 +33,7 @@
 namespace tts {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kHeads = 128;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
@@ -47,6 +47,7 @@ constexpr int kVStage = kVSlabs * kSlabBytes;        // 32 KB
 constexpr int kSmemBytes = kQhiBytes + 2 * kKStage + 2 * kVStage + 1024;
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxTiles = kMaxTopk / kTileN;         // 32
+constexpr int kCountCap = 16384;  // kv_len up to this uses a counting sort
 
 struct SparseParams {
   const uint16_t* q;  // bf16 bits [nq, 128, 576]
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_vempty[2], bar_s[2], bar_p[2], bar_o, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_cnt;
+  __shared__ int s_wsum[kThreads / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x >> 1, r = blockIdx.x & 1;
@@ -81,7 +83,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQhi = sb;
   const uint32_t sK0 = sb + kQhiBytes;
   const uint32_t sV0 = sK0 + 2 * kKStage;
-  int32_t* sort_buf = reinterpret_cast<int32_t*>(smem + kQhiBytes);  // scratch before gathering
 
   if (tid == 0) {
     s_abort = 0;
@@ -89,8 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bar_qhi), 1);
     mbar_init(smem_u32(&bar_qlo), 128);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_kfull[i]), 64);
-      mbar_init(smem_u32(&bar_vfull[i]), 64);
+      mbar_init(smem_u32(&bar_kfull[i]), 128);
+      mbar_init(smem_u32(&bar_vfull[i]), 128);
       mbar_init(smem_u32(&bar_kempty[i]), 1);
       mbar_init(smem_u32(&bar_vempty[i]), 1);
       mbar_init(smem_u32(&bar_s[i]), 1);
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bar_drain), 1);
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(smem_u32(&s_tmem), 512);
     tmem_relinquish();
   }
@@ -114,9 +115,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- canonical order: validate, then sort the index list ascending ----
+  // Scratch (the gather stages are still unused): counts [kv_len] then the sorted list.
+  int32_t* counts = reinterpret_cast<int32_t*>(smem + kQhiBytes);
+  int32_t* sorted = counts + kCountCap;
   const int32_t* idx_row = p.idx + (int64_t)n * p.topk;
+  const bool by_count = p.kv_len <= kCountCap;
+  if (by_count)
+    for (int v = tid; v < p.kv_len; v += kThreads) counts[v] = 0;
+  __syncthreads();
   int my_valid = 0;
-  for (int j = tid; j < p.sort_n; j += kThreads) {
+  for (int j = tid; j < (by_count ? p.topk : p.sort_n); j += kThreads) {
     int key = 0x7FFFFFFF;
     if (j < p.topk) {
       const int32_t i = idx_row[j];
@@ -134,37 +142,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    sort_buf[j] = key;
+    if (by_count) {
+      if (key != 0x7FFFFFFF) atomicAdd(&counts[key], 1);  // integer: order-independent
+    } else {
+      sorted[j] = key;
+    }
   }
   if (my_valid) atomicAdd(&s_cnt, my_valid);
   __syncthreads();
-  for (int size = 2; size <= p.sort_n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < (p.sort_n >> 1); i += kThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const int a = sort_buf[lo], b = sort_buf[hi];
-        if ((a > b) == asc) {
-          sort_buf[lo] = b;
-          sort_buf[hi] = a;
+  if (by_count) {
+    // Counting sort: thread t owns a contiguous range of positions; an exclusive scan
+    // of the per-range totals gives where each range's entries start.
+    const int per = (p.kv_len + kThreads - 1) / kThreads;
+    const int v0 = tid * per, v1 = min(p.kv_len, v0 + per);
+    int tot = 0;
+    for (int v = v0; v < v1; ++v) tot += counts[v];
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_wsum[w];
+    int pos = before + incl - tot;
+    for (int v = v0; v < v1; ++v)
+      for (int c = counts[v]; c > 0; --c) sorted[pos++] = v;
+  } else {
+    for (int size = 2; size <= p.sort_n; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < (p.sort_n >> 1); i += kThreads) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool asc = (lo & size) == 0;
+          const int a = sorted[lo], b = sorted[hi];
+          if ((a > b) == asc) {
+            sorted[lo] = b;
+            sorted[hi] = a;
+          }
         }
+        __syncthreads();
       }
-      __syncthreads();
     }
   }
+  __syncthreads();
   const int cnt = s_cnt;
   const int n_tiles = (cnt + kTileN - 1) / kTileN;
-  // Producer threads keep the physical row of their entry of every tile.
+  // Producer lanes 0..15 of producer warp w keep the physical row of entry
+  // 16 * (w & 3) + lane of every tile.
   int32_t my_row[kMaxTiles];
-  if (warp < 4) {
-    const int e = tid & 63;
+  if (warp < 8) {
+    const int e = 16 * (warp & 3) + (lane & 15);
 #pragma unroll
     for (int j = 0; j < kMaxTiles; ++j) {
       const int pos = j * kTileN + e;
       int32_t row = -1;
       if (pos < cnt) {
-        const int32_t i = sort_buf[pos];
+        const int32_t i = sorted[pos];
         row = p.page_table[i / p.page_size] * p.page_size + i % p.page_size;
       }
       my_row[j] = row;
@@ -176,9 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ------------------------------------------------------------ Q_lo -> TMEM, gather
-    {
+    if (warp < 4) {
       const int h = tid;  // warp w covers TMEM lanes 32w..32w+31
       const uint32_t* qrow =
           reinterpret_cast<const uint32_t*>(p.q + ((int64_t)n * kHeads + h) * kDqk);
@@ -199,32 +235,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_qlo));
     }
-    const bool kside = warp < 2;
-    const int e = tid & 63;
+    const bool kside = warp < 4;
     const int nslab = kside ? kKOnly : kVSlabs;
+    // Producer warp w of a role copies entries 16*(w&3) .. +15 of the tile. Lane l copies
+    // the 16-byte chunk (l & 7) of entry 16*(w&3) + 4*rr + (l >> 3), rr = 0..3, so one
+    // warp instruction moves four whole 128-byte row segments. Row offsets come from
+    // the lane that owns the entry (my_row), by shuffle.
+    const int e_base = 16 * (warp & 3);
+    const int chunk = lane & 7;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       if (j >= 2) {
         const uint32_t eb = smem_u32(kside ? &bar_kempty[st] : &bar_vempty[st]);
         if (!mbar_wait(eb, ((j >> 1) - 1) & 1, abort_flag, p.dev_status)) break;
       }
-      const int32_t row = my_row[j];
-      const uint16_t* src_row = p.kv + (int64_t)(row < 0 ? 0 : row) * kDqk;
-      const uint32_t src_bytes = row < 0 ? 0u : 16u;
-      const uint32_t dst_base = (kside ? sK0 + st * kKStage : sV0 + st * kVStage) + e * 128;
-      for (int i = 0; i < nslab; ++i) {
-        const int g = kside ? kslab_of(r, i) : 4 * r + i;
+      const int32_t own_row = my_row[j];
+      const uint32_t stage = kside ? sK0 + st * kKStage : sV0 + st * kVStage;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          cp_async_16(dst_base + i * kSlabBytes + ((c ^ (e & 7)) << 4), src_row + g * 64 + c * 8,
-                      src_bytes);
+      for (int rr = 0; rr < 4; ++rr) {
+        const int el = rr * 4 + (lane >> 3);  // entry within this warp's 16
+        const int32_t row = __shfl_sync(0xFFFFFFFFu, own_row, el);
+        const int e = e_base + el;
+        const uint16_t* src_row = p.kv + (int64_t)(row < 0 ? 0 : row) * kDqk + chunk * 8;
+        const uint32_t src_bytes = row < 0 ? 0u : 16u;
+        const uint32_t dst = stage + e * 128 + ((chunk ^ (e & 7)) << 4);
+        for (int i = 0; i < nslab; ++i) {
+          const int g = kside ? kslab_of(r, i) : 4 * r + i;
+          cp_async_16(dst + i * kSlabBytes, src_row + g * 64, src_bytes);
+        }
       }
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(kside ? &bar_kfull[st] : &bar_vfull[st]));
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTileN, 0, 0);
@@ -240,12 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                smem_desc(sV0 + kVStage, kSlabBytes, 1024, kSw128)};
       bool ok = mbar_wait(smem_u32(&bar_qhi), 0, abort_flag, p.dev_status) &&
                 mbar_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status);
-      // S(t) = Q K^T for tile t into S buffer t&1: K-only slabs (Q from smem), then
-      // V slabs (Q from TMEM). The order of the 36 partial products is fixed.
-      auto issue_s = [&](int t) -> bool {
+      // S(t) = Q K^T for tile t into S buffer t&1, in two parts with a fixed order:
+      // the K-only slabs (Q from shared memory), then the V slabs (Q from TMEM).
+      auto issue_s_k = [&](int t) -> bool {
         const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!mbar_wait(smem_u32(&bar_kfull[st]), ph, abort_flag, p.dev_status)) return false;
+        if (!mbar_wait(smem_u32(&bar_kfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
+          return false;
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kKOnly; ++i)
@@ -254,7 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(S_t[st], dq + ((i * kQSlabBytes + ks * 32) >> 4),
                    dk[st] + ((i * kSlabBytes + ks * 32) >> 4), idesc_s, (i | ks) != 0);
         mma_commit(smem_u32(&bar_kempty[st]));
-        if (!mbar_wait(smem_u32(&bar_vfull[st]), ph, abort_flag, p.dev_status)) return false;
+        return true;
+      };
+      auto issue_s_v = [&](int t) -> bool {
+        const int st = t & 1;
+        if (!mbar_wait(smem_u32(&bar_vfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
+          return false;
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kVSlabs; ++i)
@@ -265,9 +315,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(smem_u32(&bar_s[st]));
         return true;
       };
+      // Issue order: PV(t), S_v(t+1), S_k(t+2). The V slabs of tile t+1 were gathered
+      // while S_v(t), S_k(t+1) and PV(t) ran; softmax(t+1) overlaps S_k(t+2).
       if (ok) {
         tc_fence_after();
-        ok = issue_s(0) && (n_tiles < 2 || issue_s(1));
+        ok = issue_s_k(0) && issue_s_v(0) && (n_tiles < 2 || issue_s_k(1));
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j & 1;
@@ -279,12 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                  (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(smem_u32(&bar_vempty[st]));
         if (j + 1 == n_tiles) mma_commit(smem_u32(&bar_o));
-        if (j + 2 < n_tiles && !issue_s(j + 2)) break;
+        if (j + 1 < n_tiles && !issue_s_v(j + 1)) break;
+        if (j + 2 < n_tiles && !issue_s_k(j + 2)) break;
       }
       mma_commit(smem_u32(&bar_drain));
       mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ softmax / epilogue
     const int h = ((warp & 3) << 5) + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -309,10 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < kTileN; ++cc)
           if (cc >= valid) s[cc] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int cc = 1; cc < kTileN; ++cc) mx = fmaxf(mx, s[cc]);
-      const float m_new = fmaxf(m_ref, mx);
+      const float m_new = fmaxf(m_ref, row_max<kTileN>(s));
       const bool resc = (m_new - m_ref) * c > 8.0f;
       float alpha = 1.f;
       if (resc) {
@@ -321,22 +371,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
       }
       const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
-      float rs = 0.f;
+      float2 rs2 = make_float2(0.f, 0.f);
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_mc, neg_mc);
 #pragma unroll
       for (int cc = 0; cc < kTileN / 2; ++cc) {
-        const float p0 = ex2_approx(fmaf(s[2 * cc], c, neg_mc));
-        const float p1 = ex2_approx(fmaf(s[2 * cc + 1], c, neg_mc));
-        rs += p0 + p1;
-        sr[cc] = pack_bf16x2(p0, p1);
+        float2 x = ffma2(make_float2(s[2 * cc], s[2 * cc + 1]), c2, nm2);
+        x.x = ex2_approx(x.x);
+        x.y = ex2_approx(x.y);
+        rs2 = fadd2(rs2, x);
+        sr[cc] = pack_bf16x2(x.x, x.y);
       }
-      l += rs;
+      l += rs2.x + rs2.y;
       tmem_st32(S_row, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
       if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
-        // O must hold every PV up to tile j-1: PV(j-1) is the last one issued.
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_vempty[(j - 1) & 1]),
-                                                ((j - 1) >> 1) & 1, abort_flag, p.dev_status));
-        if (!ok) break;
-        tc_fence_after();
+        // O holds every PV up to tile j-1: PV(j-1) was issued before S_v(j), whose
+        // completion this thread has observed (one commit covers all earlier MMAs).
         const uint32_t O_row = tmem + 256 + lane_off;
 #pragma unroll 1
         for (int c0 = 0; c0 < 256; c0 += 32) {
@@ -385,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) mbar_wait(smem_u32(&bar_qhi), 0, nullptr, p.dev_status);
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
