@@ -45,14 +45,22 @@ struct AttnCfg {
   static constexpr int kBoxBytes = kBlockN * 128;  // one SW128 box of 128 rows
   static constexpr int kTailBytes = kBlockN * 32;  // one SW32 box of 128 rows
   static constexpr int kTileBytes = kMainBoxes * kBoxBytes + (kTail ? kTailBytes : 0);
+  // V for d=80 is loaded as three 32-column SW64 boxes (d 80..95 zero-filled by the
+  // tensor map's bounds) so that one N=96 MMA per K step covers it; d=64/128 reuse the
+  // K/Q layout.
+  static constexpr int kVBoxes = kTail ? 3 : kMainBoxes;
+  static constexpr int kVBoxBytes = kTail ? kBlockN * 64 : kBoxBytes;
+  static constexpr int kVTileBytes = kVBoxes * kVBoxBytes;
+  static constexpr int kPvN = kTail ? 96 : D;
   static constexpr int kStages = (D <= 80) ? 3 : 2;
-  static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
+  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + kStages * kVTileBytes + 1024;
   static_assert(kTail == 0 || kTail == 16, "head_dim must be 64, 80 or 128");
 };
 
 struct AttnMaps {
   CUtensorMap q, k, v;           // SW128 boxes {64, 1, 128}
-  CUtensorMap q_t, k_t, v_t;     // SW32 boxes {16, 1, 128} for the d=64..79 tail
+  CUtensorMap q_t, k_t;          // SW32 boxes {16, 1, 128} for the d=64..79 tail
+  CUtensorMap v_t;               // d=80: SW64 boxes {32, 1, 128} for all of V
 };
 
 struct AttnParams {
@@ -95,22 +103,18 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_d, uint64_t
   if constexpr (C::kTail != 0) mma_ss(d_tmem, q_tail_d, k_tail_d, idesc, 1);
 }
 
-// O[tmem] (+)= P[tmem] V[smem]; V is MN-major (d contiguous) in the same boxes.
+// O[tmem] (+)= P[tmem] V[smem]; V is MN-major (d contiguous). v_d describes the
+// first V box (SW128 boxes for d=64/128, SW64 boxes for d=80).
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_d,
-                                         uint64_t v_tail_d, uint32_t accumulate) {
+                                         uint32_t accumulate) {
   using C = AttnCfg<D>;
-  constexpr uint32_t idesc_main = idesc_bf16_f32(128, C::kMainBoxes * 64, 0, 1);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, C::kPvN, 0, 1);
+  constexpr uint32_t kStep = C::kTail ? 16 * 64 : 16 * 128;  // 16 key rows of one box
 #pragma unroll
-  for (int ks = 0; ks < kBlockN / 16; ++ks) {
-    const uint32_t acc = (ks > 0) ? 1u : accumulate;
-    mma_ts(o_tmem, p_tmem + ks * 8, v_d + ((ks * 2048) >> 4), idesc_main, acc);
-    if constexpr (C::kTail != 0) {
-      constexpr uint32_t idesc_tail = idesc_bf16_f32(128, 16, 0, 1);
-      mma_ts(o_tmem + C::kMainBoxes * 64, p_tmem + ks * 8, v_tail_d + ((ks * 512) >> 4),
-             idesc_tail, acc);
-    }
-  }
+  for (int ks = 0; ks < kBlockN / 16; ++ks)
+    mma_ts(o_tmem, p_tmem + ks * 8, v_d + ((ks * kStep) >> 4), idesc,
+           (ks > 0) ? 1u : accumulate);
 }
 
 template <int D>
@@ -157,7 +161,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sQ[2] = {s_base, s_base + C::kTileBytes};
   auto sK = [&](int st) { return s_base + (2 + st) * C::kTileBytes; };
-  auto sV = [&](int st) { return s_base + (2 + NS + st) * C::kTileBytes; };
+  auto sV = [&](int st) {
+    return s_base + (2 + NS) * C::kTileBytes + st * C::kVTileBytes;
+  };
 
   if (tid == 0) {
     s_abort = 0;
@@ -206,8 +212,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int tok = (int)(k_start + (int64_t)j * kBlockN);
         mbar_arrive_expect_tx(smem_u32(&bar_k[st]), C::kTileBytes);
         load_tile<D>(sK(st), &maps.k, &maps.k_t, smem_u32(&bar_k[st]), g, tok);
-        mbar_arrive_expect_tx(smem_u32(&bar_v[st]), C::kTileBytes);
-        load_tile<D>(sV(st), &maps.v, &maps.v_t, smem_u32(&bar_v[st]), g, tok);
+        mbar_arrive_expect_tx(smem_u32(&bar_v[st]), C::kVTileBytes);
+        if constexpr (C::kTail != 0) {
+#pragma unroll
+          for (int b = 0; b < C::kVBoxes; ++b)
+            tma_load_3d(sV(st) + b * C::kVBoxBytes, &maps.v_t, smem_u32(&bar_v[st]), b * 32, g,
+                        tok);
+        } else {
+          load_tile<D>(sV(st), &maps.v, &maps.v, smem_u32(&bar_v[st]), g, tok);
+        }
         issued = j + 1;
       }
       if (*abort_flag && n_tiles > 0) {
@@ -225,7 +238,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t S_t[2] = {tmem, tmem + 128};
       const uint32_t O_t[2] = {tmem + 256, tmem + 384};
       constexpr uint32_t kTailOff = C::kMainBoxes * C::kBoxBytes;
-      uint64_t qd[2], qtd[2], kd[NS], ktd[NS], vd[NS], vtd[NS];
+      uint64_t qd[2], qtd[2], kd[NS], ktd[NS], vd[NS];
       for (int w = 0; w < 2; ++w) {
         qd[w] = smem_desc(sQ[w], 16, 1024, kSw128);
         qtd[w] = smem_desc(sQ[w] + kTailOff, 16, 256, kSw32);
@@ -233,8 +246,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int i = 0; i < NS; ++i) {
         kd[i] = smem_desc(sK(i), 16, 1024, kSw128);
         ktd[i] = smem_desc(sK(i) + kTailOff, 16, 256, kSw32);
-        vd[i] = smem_desc(sV(i), C::kBoxBytes, 1024, kSw128);
-        vtd[i] = smem_desc(sV(i) + kTailOff, C::kTailBytes, 256, kSw32);
+        vd[i] = C::kTail ? smem_desc(sV(i), C::kVBoxBytes, 512, kSw64)
+                         : smem_desc(sV(i), C::kBoxBytes, 1024, kSw128);
       }
       bool ok = mbar_wait(smem_u32(&bar_q), 0, abort_flag, p.dev_status) &&
                 mbar_wait(smem_u32(&bar_k[0]), 0, abort_flag, p.dev_status);
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // warpgroup 0
         if (!mbar_wait(smem_u32(&bar_p[0]), j & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
-        issue_pv<D>(O_t[0], S_t[0], vd[st], vtd[st], j > 0);
+        issue_pv<D>(O_t[0], S_t[0], vd[st], j > 0);
         if (more) {
           if (!mbar_wait(smem_u32(&bar_k[st1]), ph1, abort_flag, p.dev_status)) break;
           tc_fence_after();
@@ -267,7 +280,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // warpgroup 1
         if (!mbar_wait(smem_u32(&bar_p[1]), j & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
-        issue_pv<D>(O_t[1], S_t[1], vd[st], vtd[st], j > 0);
+        issue_pv<D>(O_t[1], S_t[1], vd[st], j > 0);
         mma_commit(smem_u32(&bar_kv_empty[st]));
         if (more) {
           issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1]);
@@ -431,7 +444,7 @@ cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
   if constexpr (C::kTail != 0) {
     if (!make(&maps.q_t, a.q, tq, a.hq, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
         !make(&maps.k_t, a.k, tk, a.hkv, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make(&maps.v_t, a.v, tk, a.hkv, 16, CU_TENSOR_MAP_SWIZZLE_32B))
+        !make(&maps.v_t, a.v, tk, a.hkv, 32, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   } else {
     maps.q_t = maps.q;
