@@ -159,6 +159,15 @@ tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, i
                                  uint32_t* dev_status, void* stream);
 
 /*
+ * Diagnostics (no counterpart in the pages): launches one thread that waits on a
+ * barrier phase nothing completes. The wait is bounded like every wait in the library:
+ * after about one second it ORs TTS_DEV_TIMEOUT into *dev_status (device pointer,
+ * required) and the kernel returns, leaving the CUDA context usable. Used by the
+ * test-suite to check the timeout path without faulting or hanging the GPU.
+ */
+tts_status tts_debug_wait_timeout(uint32_t* dev_status, void* stream);
+
+/*
  * Allocation-free variant of tts_attn_fwd_varlen for fp32 q / k / v.
  *
  * This entry point has no counterpart in the pages; it exists for callers that

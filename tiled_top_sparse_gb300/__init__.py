@@ -46,6 +46,7 @@ EXPORTED = (
     "tts_topk_select",
     "tts_sparse_attn_paged",
     "tts_attn_fwd_varlen_f32_noalloc",
+    "tts_debug_wait_timeout",
 )
 
 
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
     L.tts_attn_fwd_varlen_f32_noalloc.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, i32,
                                                   i32, i32, i32, f32, P, P, P, P]
     L.tts_attn_fwd_varlen_f32_noalloc.restype = ctypes.c_int
+    L.tts_debug_wait_timeout.argtypes = [P, P]
+    L.tts_debug_wait_timeout.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -123,6 +126,13 @@ def check_status(status: torch.Tensor, what: str = "device status"):
     """Synchronise on `status` (1-element int32 CUDA tensor) and raise if a flag is set."""
     v = int(status.item()) & 0xFFFFFFFF
     _check(lib().tts_status_from_device(ctypes.c_uint32(v)), what)
+
+
+def debug_wait_timeout(status: torch.Tensor):
+    """Run the library's bounded-wait self-test kernel (see tts_debug_wait_timeout)."""
+    _cuda_contig(status, "status", torch.int32)
+    _check(lib().tts_debug_wait_timeout(_ptr(status), _stream(status.device)),
+           "tts_debug_wait_timeout")
 
 
 def attn_workspace_bytes(total_q, total_k, num_heads_q, num_heads_kv, head_dim, dtype) -> int:
