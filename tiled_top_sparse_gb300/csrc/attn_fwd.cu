@@ -190,7 +190,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -337,19 +336,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_ref = m_new;
       }
       const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
-      // P packed as bf16 pairs into sr[0..63] (slot cc is written after s[2cc], s[2cc+1]
-      // were read, so the in-place reuse is safe). Two partial row sums, added at the end.
-      float2 rs2 = make_float2(0.f, 0.f);
-      const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_mc, neg_mc);
-#pragma unroll
-      for (int cc = 0; cc < 64; ++cc) {
-        float2 x = ffma2(make_float2(s[2 * cc], s[2 * cc + 1]), c2, nm2);
-        x.x = ex2_approx(x.x);
-        x.y = ex2_approx(x.y);
-        rs2 = fadd2(rs2, x);
-        sr[cc] = pack_bf16x2(x.x, x.y);
-      }
-      l += rs2.x + rs2.y;
+      // P packed as bf16 pairs over sr[0..63], in place.
+      l += exp2_pack_sum<128>(sr, c, neg_mc);
 #pragma unroll
       for (int q4 = 0; q4 < 2; ++q4)
         tmem_st32(S_row + q4 * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[q4 * 32]));
@@ -374,29 +362,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (ok && n_tiles > 0)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_o[wg]), 0, abort_flag, p.dev_status));
     tc_fence_after();
-    const bool store = ok && i < Lq;
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    float* orow = p.out + ((q_start + i) * p.hq + h) * (int64_t)D;
-    if (n_tiles > 0 && ok) {
+    if (ok) {
+      // Rows leave TMEM one per thread; a 4 KB slice of this warpgroup's Q tile (no
+      // MMA reads it any more: bar_o covers every MMA issued for this tile) turns them
+      // into whole 128-byte row segments, so each store instruction writes full lines.
+      float4* stage = reinterpret_cast<float4*>(smem + wg * C::kTileBytes + (warp & 3) * 4096);
+      const int64_t row0 = q_lo + wg * kBlockM + (warp & 3) * 32;  // this warp's first row
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t o[16];
-        tmem_ld16(O_row + c0, o);
-        tmem_ld_wait();
-        if (store) {
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            float4 v4 = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
-                                    __uint_as_float(o[e + 2]) * inv_l,
-                                    __uint_as_float(o[e + 3]) * inv_l);
-            *reinterpret_cast<float4*>(orow + c0 + e) = v4;
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        constexpr int kW = 32;
+        const int w = (D - c0 < kW) ? D - c0 : kW;  // 32, or 16 for the d = 80 tail
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          if (w == 32) {
+            tmem_ld32(O_row + c0, o);
+          } else {
+            tmem_ld16(O_row + c0, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
           }
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < w / 4)
+            stage[lane * 8 + (q ^ (lane & 7))] =
+                make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                            __uint_as_float(o[4 * q + 2]) * inv_l,
+                            __uint_as_float(o[4 * q + 3]) * inv_l);
+        __syncwarp();
+        const int lpr = w / 4;  // lanes per row segment
+        for (int rr = 0; rr < 32; rr += 32 / lpr) {
+          const int r = rr + lane / lpr, q = lane % lpr;
+          const float4 v = stage[r * 8 + (q ^ (r & 7))];
+          const int64_t ii = row0 + r;
+          if (ii < Lq)
+            *reinterpret_cast<float4*>(p.out + ((q_start + ii) * p.hq + h) * (int64_t)D + c0 +
+                                       4 * q) = v;
+        }
+        __syncwarp();
       }
-    } else if (store) {
-      for (int c0 = 0; c0 < D; c0 += 4)
-        *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    const bool store = ok && i < Lq;
     if (store && p.lse != nullptr)
       p.lse[(q_start + i) * p.hq + h] =
           (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
@@ -471,8 +480,8 @@ cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
   const int64_t grid = (int64_t)a.batch * p.pairs_max * a.hq;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes);
   if (e != cudaSuccess) return e;
   attn_fwd_kernel<D><<<(unsigned)grid, kAttnThreads, C::kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();

@@ -317,7 +317,7 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
 // ---------------------------------------------------------------- misc math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 // Packed two-lane fp32 arithmetic (one instruction for two values).
@@ -354,22 +354,55 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// Row max of n values (n a multiple of 2) with three-input max.
+// Row max of N values (N a multiple of 16): eight independent three-input max
+// chains, so the reduction's latency is N/16 steps instead of N/4.
 template <int N>
 __device__ __forceinline__ float row_max(const float* s) {
-  float m0 = s[0], m1 = s[1];
+  static_assert(N % 16 == 0, "row_max needs a multiple of 16 values");
+  float mm[8];
 #pragma unroll
-  for (int i = 2; i + 3 < N; i += 4) {
-    m0 = fmax3(m0, s[i], s[i + 1]);
-    m1 = fmax3(m1, s[i + 2], s[i + 3]);
-  }
-  if constexpr ((N - 2) % 4 != 0) m0 = fmax3(m0, s[N - 2], s[N - 1]);
-  return fmaxf(m0, m1);
+  for (int t = 0; t < 8; ++t) mm[t] = fmaxf(s[2 * t], s[2 * t + 1]);
+#pragma unroll
+  for (int i = 16; i < N; i += 16)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) mm[t] = fmax3(mm[t], s[i + 2 * t], s[i + 2 * t + 1]);
+  return fmaxf(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], fmax3(mm[5], mm[6], mm[7])));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits), .y = hi
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// p = 2^(s * c + nmc) for N scores, packed as bf16 pairs into sr[0 .. N/2) (in place:
+// sr aliases s, and pair slot k is written only after s[2k], s[2k+1] were read);
+// returns the fp32 sum of the unrounded p. Eight pairs per batch and four partial
+// sums keep several exponentials in flight for one warp.
+template <int N>
+__device__ __forceinline__ float exp2_pack_sum(uint32_t* sr, float c, float nmc) {
+  static_assert(N % 16 == 0, "exp2_pack_sum needs a multiple of 16 values");
+  const float* s = reinterpret_cast<const float*>(sr);
+  const float2 c2 = make_float2(c, c), nm2 = make_float2(nmc, nmc);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int k0 = 0; k0 < N / 2; k0 += 8) {
+    float2 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      x[u] = ffma2(make_float2(s[2 * (k0 + u)], s[2 * (k0 + u) + 1]), c2, nm2);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      x[u].x = ex2_approx(x[u].x);
+      x[u].y = ex2_approx(x[u].y);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u & 3] = fadd2(acc[u & 3], x[u]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sr[k0 + u] = pack_bf16x2(x[u].x, x[u].y);
+  }
+  const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  return a.x + a.y;
 }
 
 }  // namespace tts
