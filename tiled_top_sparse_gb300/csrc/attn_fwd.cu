@@ -11,7 +11,8 @@
 //
 // How (one CTA = one (sequence, 256-row query pair, head)):
 //   warp 0        TMA producer: Q tiles once, then K/V 128-row tiles into a ring
-//   warp 1        TMEM allocator + single-thread tcgen05 MMA issuer
+//   warp 1        TMEM allocator + tcgen05 MMA issuer (the whole warp runs the
+//                 issue loop converged; one elected lane issues)
 //   warps 4..7    softmax warpgroup 0 (query rows 0..127 of the pair)
 //   warps 8..11   softmax warpgroup 1 (query rows 128..255)
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D).
@@ -90,31 +91,40 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* main,
 // S[tmem] = Q[smem] K[smem]^T over the D-deep contraction. q_d / k_d are the
 // descriptors of the tiles' first box; every other K step is a constant offset
 // (the 14-bit start-address field never carries: shared addresses are < 256 KB).
+// e: the elected lane of the converged issuing warp.
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_d, uint64_t k_d,
-                                         uint64_t q_tail_d, uint64_t k_tail_d) {
+                                         uint64_t q_tail_d, uint64_t k_tail_d, uint32_t e) {
   using C = AttnCfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(128, kBlockN, 0, 0);
 #pragma unroll
   for (int ks = 0; ks < C::kMainBoxes * 4; ++ks) {
     const uint32_t off = ((ks / 4) * C::kBoxBytes + (ks % 4) * 32) >> 4;
-    mma_ss(d_tmem, q_d + off, k_d + off, idesc, ks > 0);
+    mma_ss_elect(d_tmem, q_d + off, k_d + off, idesc, ks > 0, e);
   }
-  if constexpr (C::kTail != 0) mma_ss(d_tmem, q_tail_d, k_tail_d, idesc, 1);
+  if constexpr (C::kTail != 0) mma_ss_elect(d_tmem, q_tail_d, k_tail_d, idesc, 1, e);
 }
 
 // O[tmem] (+)= P[tmem] V[smem]; V is MN-major (d contiguous). v_d describes the
 // first V box (SW128 boxes for d=64/128, SW64 boxes for d=80).
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_d,
-                                         uint32_t accumulate) {
+                                         uint32_t accumulate, uint32_t e) {
   using C = AttnCfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(128, C::kPvN, 0, 1);
   constexpr uint32_t kStep = C::kTail ? 16 * 64 : 16 * 128;  // 16 key rows of one box
 #pragma unroll
   for (int ks = 0; ks < kBlockN / 16; ++ks)
-    mma_ts(o_tmem, p_tmem + ks * 8, v_d + ((ks * kStep) >> 4), idesc,
-           (ks > 0) ? 1u : accumulate);
+    mma_ts_elect(o_tmem, p_tmem + ks * 8, v_d + ((ks * kStep) >> 4), idesc,
+                 (ks > 0) ? 1u : accumulate, e);
+}
+
+// Wait for a barrier that is usually complete already: a cheap non-blocking look
+// first, then the bounded wait. Warp-collective (the result is the warp's AND).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  bool ok = mbar_peek(bar, parity) || mbar_wait(bar, parity, abort, status);
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 template <int D>
@@ -123,6 +133,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   using C = AttnCfg<D>;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
+  // bar_k / bar_v: K and V of a tile landed. With three stages (d <= 80) the V load
+  // has time to land before the S MMA that first needs the tile, so both share bar_k
+  // and the MMA warp waits once per tile; with two stages (d = 128) V gets its own
+  // barrier so S(j+1) does not wait for V(j+1).
+  constexpr bool kOneKV = NS >= 3;
   __shared__ __align__(8) uint64_t bar_q, bar_k[NS], bar_v[NS], bar_kv_empty[NS], bar_s[2],
       bar_p[2], bar_o[2], bar_drain;
   __shared__ uint32_t s_tmem;
@@ -209,16 +224,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             !mbar_wait(smem_u32(&bar_kv_empty[st]), ((j / NS) - 1) & 1, abort_flag, p.dev_status))
           break;
         const int tok = (int)(k_start + (int64_t)j * kBlockN);
-        mbar_arrive_expect_tx(smem_u32(&bar_k[st]), C::kTileBytes);
-        load_tile<D>(sK(st), &maps.k, &maps.k_t, smem_u32(&bar_k[st]), g, tok);
-        mbar_arrive_expect_tx(smem_u32(&bar_v[st]), C::kVTileBytes);
+        const uint32_t bk = smem_u32(&bar_k[st]);
+        const uint32_t bv = kOneKV ? bk : smem_u32(&bar_v[st]);
+        if (kOneKV) {
+          mbar_arrive_expect_tx(bk, C::kTileBytes + C::kVTileBytes);
+        } else {
+          mbar_arrive_expect_tx(bk, C::kTileBytes);
+          mbar_arrive_expect_tx(bv, C::kVTileBytes);
+        }
+        load_tile<D>(sK(st), &maps.k, &maps.k_t, bk, g, tok);
         if constexpr (C::kTail != 0) {
 #pragma unroll
           for (int b = 0; b < C::kVBoxes; ++b)
-            tma_load_3d(sV(st) + b * C::kVBoxBytes, &maps.v_t, smem_u32(&bar_v[st]), b * 32, g,
-                        tok);
+            tma_load_3d(sV(st) + b * C::kVBoxBytes, &maps.v_t, bv, b * 32, g, tok);
         } else {
-          load_tile<D>(sV(st), &maps.v, &maps.v, smem_u32(&bar_v[st]), g, tok);
+          load_tile<D>(sV(st), &maps.v, &maps.v, bv, g, tok);
         }
         issued = j + 1;
       }
@@ -227,13 +247,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_wait(bq, 0, nullptr, nullptr);
         for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j) {
           mbar_wait(smem_u32(&bar_k[j % NS]), (j / NS) & 1, nullptr, nullptr);
-          mbar_wait(smem_u32(&bar_v[j % NS]), (j / NS) & 1, nullptr, nullptr);
+          if (!kOneKV) mbar_wait(smem_u32(&bar_v[j % NS]), (j / NS) & 1, nullptr, nullptr);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    if (n_tiles > 0) {
+      const uint32_t e = elect_one();
       const uint32_t S_t[2] = {tmem, tmem + 128};
       const uint32_t O_t[2] = {tmem + 256, tmem + 384};
       constexpr uint32_t kTailOff = C::kMainBoxes * C::kBoxBytes;
@@ -248,48 +269,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         vd[i] = C::kTail ? smem_desc(sV(i), C::kVBoxBytes, 512, kSw64)
                          : smem_desc(sV(i), C::kBoxBytes, 1024, kSw128);
       }
-      bool ok = mbar_wait(smem_u32(&bar_q), 0, abort_flag, p.dev_status) &&
-                mbar_wait(smem_u32(&bar_k[0]), 0, abort_flag, p.dev_status);
+      bool ok = warp_wait(smem_u32(&bar_q), 0, abort_flag, p.dev_status) &&
+                warp_wait(smem_u32(&bar_k[0]), 0, abort_flag, p.dev_status);
       if (ok) {
         tc_fence_after();
-        issue_qk<D>(S_t[0], qd[0], kd[0], qtd[0], ktd[0]);
-        mma_commit(smem_u32(&bar_s[0]));
-        issue_qk<D>(S_t[1], qd[1], kd[0], qtd[1], ktd[0]);
-        mma_commit(smem_u32(&bar_s[1]));
+        issue_qk<D>(S_t[0], qd[0], kd[0], qtd[0], ktd[0], e);
+        mma_commit_elect(smem_u32(&bar_s[0]), e);
+        issue_qk<D>(S_t[1], qd[1], kd[0], qtd[1], ktd[0], e);
+        mma_commit_elect(smem_u32(&bar_s[1]), e);
       }
+      // Order on the tensor core: PV0(j) S0(j+1) PV1(j) S1(j+1).
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % NS;
-        const uint32_t ph = (j / NS) & 1;
         const bool more = j + 1 < n_tiles;
         const int st1 = (j + 1) % NS;
-        const uint32_t ph1 = ((j + 1) / NS) & 1;
-        if (!mbar_wait(smem_u32(&bar_v[st]), ph, abort_flag, p.dev_status)) break;
+        if (!kOneKV && !warp_wait(smem_u32(&bar_v[st]), (j / NS) & 1, abort_flag, p.dev_status))
+          break;
         // warpgroup 0
-        if (!mbar_wait(smem_u32(&bar_p[0]), j & 1, abort_flag, p.dev_status)) break;
+        if (!warp_wait(smem_u32(&bar_p[0]), j & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
-        issue_pv<D>(O_t[0], S_t[0], vd[st], j > 0);
+        issue_pv<D>(O_t[0], S_t[0], vd[st], j > 0, e);
         if (more) {
-          if (!mbar_wait(smem_u32(&bar_k[st1]), ph1, abort_flag, p.dev_status)) break;
+          if (!warp_wait(smem_u32(&bar_k[st1]), ((j + 1) / NS) & 1, abort_flag, p.dev_status))
+            break;
           tc_fence_after();
-          issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1]);
-          mma_commit(smem_u32(&bar_s[0]));
+          issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
+          mma_commit_elect(smem_u32(&bar_s[0]), e);
         } else {
-          mma_commit(smem_u32(&bar_o[0]));
+          mma_commit_elect(smem_u32(&bar_o[0]), e);
         }
         // warpgroup 1
-        if (!mbar_wait(smem_u32(&bar_p[1]), j & 1, abort_flag, p.dev_status)) break;
+        if (!warp_wait(smem_u32(&bar_p[1]), j & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
-        issue_pv<D>(O_t[1], S_t[1], vd[st], j > 0);
-        mma_commit(smem_u32(&bar_kv_empty[st]));
+        issue_pv<D>(O_t[1], S_t[1], vd[st], j > 0, e);
+        mma_commit_elect(smem_u32(&bar_kv_empty[st]), e);
         if (more) {
-          issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1]);
-          mma_commit(smem_u32(&bar_s[1]));
+          issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
+          mma_commit_elect(smem_u32(&bar_s[1]), e);
         } else {
-          mma_commit(smem_u32(&bar_o[1]));
+          mma_commit_elect(smem_u32(&bar_o[1]), e);
         }
       }
-      // Drain: every MMA issued by this thread is complete before TMEM is freed.
-      mma_commit(smem_u32(&bar_drain));
+      // Drain: every MMA issued by this warp is complete before TMEM is freed.
+      mma_commit_elect(smem_u32(&bar_drain), e);
       mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
     }
   } else if (warp >= 4) {
