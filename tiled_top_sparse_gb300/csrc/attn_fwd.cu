@@ -337,19 +337,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[128];
+      float part_max[4];  // TMEM returns each 32-column chunk's max with the data
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
-        tmem_ld32(S_row + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
+        part_max[q4] =
+            tmem_ld32_max(S_row + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
       tmem_ld_wait();
       float* s = reinterpret_cast<float*>(sr);
       const int64_t kv0 = (int64_t)j * kBlockN;
-      if (kv0 + kBlockN > limit) {
+      float tile_max = fmaxf(fmax3(part_max[0], part_max[1], part_max[2]), part_max[3]);
+      if (kv0 + kBlockN > limit) {  // masked columns must not count in the max
         const int64_t lim = limit - kv0;
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc)
           if (cc >= lim) s[cc] = -INFINITY;
+        tile_max = row_max<128>(s);
       }
-      const float m_new = fmaxf(m_ref, row_max<128>(s));
+      const float m_new = fmaxf(m_ref, tile_max);
       const bool resc = (m_new - m_ref) * c > 8.0f;  // false for -inf - -inf (NaN)
       float alpha = 1.f;
       if (resc) {
