@@ -119,13 +119,6 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
                  (ks > 0) ? 1u : accumulate, e);
 }
 
-// Wait for a barrier that is usually complete already: a cheap non-blocking look
-// first, then the bounded wait. Warp-collective (the result is the warp's AND).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
-  bool ok = mbar_peek(bar, parity) || mbar_wait(bar, parity, abort, status);
-  return __all_sync(0xFFFFFFFFu, ok);
-}
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)

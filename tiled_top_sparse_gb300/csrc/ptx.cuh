@@ -109,6 +109,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Wait for a barrier that is usually complete already: a cheap non-blocking look
+// first, then the bounded wait. Warp-collective (the result is the warp's AND).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  bool ok = mbar_peek(bar, parity) || mbar_wait(bar, parity, abort, status);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

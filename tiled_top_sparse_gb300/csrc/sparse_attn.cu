@@ -271,7 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    // The whole warp runs the issue loop converged; the elected lane issues.
+    if (n_tiles > 0) {
+      const uint32_t e = elect_one();
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTileN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, 0, 1);
       const uint32_t S_t[2] = {tmem + 128, tmem + 192};
@@ -283,36 +285,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                                smem_desc(sV0 + kVStage, 16, 1024, kSw128)};
       const uint64_t dvn[2] = {smem_desc(sV0, kSlabBytes, 1024, kSw128),
                                smem_desc(sV0 + kVStage, kSlabBytes, 1024, kSw128)};
-      bool ok = mbar_wait(smem_u32(&bar_qhi), 0, abort_flag, p.dev_status) &&
-                mbar_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status);
+      bool ok = warp_wait(smem_u32(&bar_qhi), 0, abort_flag, p.dev_status) &&
+                warp_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status);
       // S(t) = Q K^T for tile t into S buffer t&1, in two parts with a fixed order:
       // the K-only slabs (Q from shared memory), then the V slabs (Q from TMEM).
       auto issue_s_k = [&](int t) -> bool {
         const int st = t & 1;
-        if (!mbar_wait(smem_u32(&bar_kfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
+        if (!warp_wait(smem_u32(&bar_kfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
           return false;
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kKOnly; ++i)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ss(S_t[st], dq + ((i * kQSlabBytes + ks * 32) >> 4),
-                   dk[st] + ((i * kSlabBytes + ks * 32) >> 4), idesc_s, (i | ks) != 0);
-        mma_commit(smem_u32(&bar_kempty[st]));
+            mma_ss_elect(S_t[st], dq + ((i * kQSlabBytes + ks * 32) >> 4),
+                         dk[st] + ((i * kSlabBytes + ks * 32) >> 4), idesc_s, (i | ks) != 0, e);
+        mma_commit_elect(smem_u32(&bar_kempty[st]), e);
         return true;
       };
       auto issue_s_v = [&](int t) -> bool {
         const int st = t & 1;
-        if (!mbar_wait(smem_u32(&bar_vfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
+        if (!warp_wait(smem_u32(&bar_vfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
           return false;
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kVSlabs; ++i)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ts(S_t[st], tmem + i * 32 + ks * 8, dvk[st] + ((i * kSlabBytes + ks * 32) >> 4),
-                   idesc_s, 1);
-        mma_commit(smem_u32(&bar_s[st]));
+            mma_ts_elect(S_t[st], tmem + i * 32 + ks * 8,
+                         dvk[st] + ((i * kSlabBytes + ks * 32) >> 4), idesc_s, 1, e);
+        mma_commit_elect(smem_u32(&bar_s[st]), e);
         return true;
       };
       // Issue order: PV(t), S_v(t+1), S_k(t+2). The V slabs of tile t+1 were gathered
@@ -323,18 +325,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(smem_u32(&bar_p[st]), (j >> 1) & 1, abort_flag, p.dev_status)) break;
+        if (!warp_wait(smem_u32(&bar_p[st]), (j >> 1) & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTileN / 16; ++ks)
-          mma_ts(O_t, S_t[st] + ks * 8, dvn[st] + ((ks * 2048) >> 4), idesc_pv,
-                 (j > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bar_vempty[st]));
-        if (j + 1 == n_tiles) mma_commit(smem_u32(&bar_o));
+          mma_ts_elect(O_t, S_t[st] + ks * 8, dvn[st] + ((ks * 2048) >> 4), idesc_pv,
+                       (j > 0 || ks > 0) ? 1u : 0u, e);
+        mma_commit_elect(smem_u32(&bar_vempty[st]), e);
+        if (j + 1 == n_tiles) mma_commit_elect(smem_u32(&bar_o), e);
         if (j + 1 < n_tiles && !issue_s_v(j + 1)) break;
         if (j + 2 < n_tiles && !issue_s_k(j + 2)) break;
       }
-      mma_commit(smem_u32(&bar_drain));
+      mma_commit_elect(smem_u32(&bar_drain), e);
       mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
     }
   } else if (warp >= 12) {
@@ -352,17 +354,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld32(S_row, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(S_row + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      const float pm0 = tmem_ld32_max(S_row, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      const float pm1 = tmem_ld32_max(S_row + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
       float* s = reinterpret_cast<float*>(sr);
       const int valid = cnt - j * kTileN;  // entries of this tile that exist
-      if (valid < kTileN) {
+      float tile_max = fmaxf(pm0, pm1);
+      if (valid < kTileN) {  // entries past the list must not count in the max
 #pragma unroll
         for (int cc = 0; cc < kTileN; ++cc)
           if (cc >= valid) s[cc] = -INFINITY;
+        tile_max = row_max<kTileN>(s);
       }
-      const float m_new = fmaxf(m_ref, row_max<kTileN>(s));
+      const float m_new = fmaxf(m_ref, tile_max);
       const bool resc = (m_new - m_ref) * c > 8.0f;
       float alpha = 1.f;
       if (resc) {
@@ -371,17 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
       }
       const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
-      float2 rs2 = make_float2(0.f, 0.f);
-      const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_mc, neg_mc);
-#pragma unroll
-      for (int cc = 0; cc < kTileN / 2; ++cc) {
-        float2 x = ffma2(make_float2(s[2 * cc], s[2 * cc + 1]), c2, nm2);
-        x.x = ex2_approx(x.x);
-        x.y = ex2_approx(x.y);
-        rs2 = fadd2(rs2, x);
-        sr[cc] = pack_bf16x2(x.x, x.y);
-      }
-      l += rs2.x + rs2.y;
+      l += exp2_pack_sum<kTileN>(sr, c, neg_mc);  // P as bf16 pairs over sr[0..31]
       tmem_st32(S_row, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
       if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
         // O holds every PV up to tile j-1: PV(j-1) was issued before S_v(j), whose
