@@ -129,10 +129,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // bar_k / bar_v: K and V of a tile landed. With three stages (d <= 80) the V load
   // has time to land before the S MMA that first needs the tile, so both share bar_k
   // and the MMA warp waits once per tile; with two stages (d = 128) V gets its own
-  // barrier so S(j+1) does not wait for V(j+1).
+  // barrier so S(j+1) does not wait for V(j+1), and K's slot is released (bar_k_empty)
+  // as soon as both S MMAs of its tile are done, a PV pair before V's slot
+  // (bar_kv_empty), so the next K load starts that much earlier.
   constexpr bool kOneKV = NS >= 3;
-  __shared__ __align__(8) uint64_t bar_q, bar_k[NS], bar_v[NS], bar_kv_empty[NS], bar_s[2],
-      bar_p[2], bar_o[2], bar_drain;
+  __shared__ __align__(8) uint64_t bar_q, bar_k[NS], bar_v[NS], bar_k_empty[NS],
+      bar_kv_empty[NS], bar_s[2], bar_p[2], bar_o[2], bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bar_k[i]), 1);
       mbar_init(smem_u32(&bar_v[i]), 1);
+      mbar_init(smem_u32(&bar_k_empty[i]), 1);
       mbar_init(smem_u32(&bar_kv_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -210,22 +213,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int w = 0; w < 2; ++w)
           load_tile<D>(sQ[w], &maps.q, &maps.q_t, bq, h, (int)(q_start + q_lo + w * kBlockM));
       }
-      int issued = 0;
+      int issued = 0, issued_v = 0;  // tiles whose K / V copies were started
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NS;
-        if (j >= NS &&
-            !mbar_wait(smem_u32(&bar_kv_empty[st]), ((j / NS) - 1) & 1, abort_flag, p.dev_status))
+        const uint32_t empty_ph = ((j / NS) - 1) & 1;
+        if (j >= NS && !mbar_wait(smem_u32(kOneKV ? &bar_kv_empty[st] : &bar_k_empty[st]),
+                                  empty_ph, abort_flag, p.dev_status))
           break;
         const int tok = (int)(k_start + (int64_t)j * kBlockN);
         const uint32_t bk = smem_u32(&bar_k[st]);
         const uint32_t bv = kOneKV ? bk : smem_u32(&bar_v[st]);
-        if (kOneKV) {
-          mbar_arrive_expect_tx(bk, C::kTileBytes + C::kVTileBytes);
-        } else {
-          mbar_arrive_expect_tx(bk, C::kTileBytes);
+        mbar_arrive_expect_tx(bk, kOneKV ? C::kTileBytes + C::kVTileBytes : C::kTileBytes);
+        load_tile<D>(sK(st), &maps.k, &maps.k_t, bk, g, tok);
+        if (!kOneKV) {
+          issued = j + 1;  // K of this tile is in flight
+          if (j >= NS &&
+              !mbar_wait(smem_u32(&bar_kv_empty[st]), empty_ph, abort_flag, p.dev_status))
+            break;
           mbar_arrive_expect_tx(bv, C::kVTileBytes);
         }
-        load_tile<D>(sK(st), &maps.k, &maps.k_t, bk, g, tok);
         if constexpr (C::kTail != 0) {
 #pragma unroll
           for (int b = 0; b < C::kVBoxes; ++b)
@@ -233,14 +239,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         } else {
           load_tile<D>(sV(st), &maps.v, &maps.v, bv, g, tok);
         }
-        issued = j + 1;
+        issued = issued_v = j + 1;
       }
       if (*abort_flag && n_tiles > 0) {
         // Best-effort drain of copies still in flight before the CTA can exit.
         mbar_wait(bq, 0, nullptr, nullptr);
         for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j) {
           mbar_wait(smem_u32(&bar_k[j % NS]), (j / NS) & 1, nullptr, nullptr);
-          if (!kOneKV) mbar_wait(smem_u32(&bar_v[j % NS]), (j / NS) & 1, nullptr, nullptr);
+          if (!kOneKV && j < issued_v)
+            mbar_wait(smem_u32(&bar_v[j % NS]), (j / NS) & 1, nullptr, nullptr);
         }
       }
     }
@@ -270,6 +277,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mma_commit_elect(smem_u32(&bar_s[0]), e);
         issue_qk<D>(S_t[1], qd[1], kd[0], qtd[1], ktd[0], e);
         mma_commit_elect(smem_u32(&bar_s[1]), e);
+        if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[0]), e);
       }
       // Order on the tensor core: PV0(j) S0(j+1) PV1(j) S1(j+1).
       for (int j = 0; ok && j < n_tiles; ++j) {
@@ -299,6 +307,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (more) {
           issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
           mma_commit_elect(smem_u32(&bar_s[1]), e);
+          if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
         } else {
           mma_commit_elect(smem_u32(&bar_o[1]), e);
         }
