@@ -86,7 +86,11 @@ int tts_version(void);
  *      [total_q, num_heads_q] (may be NULL). Rows of q not covered by any
  *      sequence are left untouched.
  * workspace  device scratch of at least tts_attn_workspace_bytes(...) bytes
- *      (16-byte aligned); may be NULL when that size is 0.
+ *      (16-byte aligned), owned by the caller and not used after the stream
+ *      reaches the end of this call: 256 bytes for the persistent kernel's
+ *      work-item counter (zeroed on the stream by the call itself), plus the
+ *      bf16 copies of q, k and v when in_dtype is TTS_F32. Concurrent calls
+ *      need separate workspaces. Missing or smaller: TTS_ERR_WORKSPACE.
  * q, k, v must be 16-byte aligned.
  */
 size_t tts_attn_workspace_bytes(int64_t total_q, int64_t total_k, int32_t num_heads_q,

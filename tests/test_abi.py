@@ -47,9 +47,10 @@ def test_status_strings_and_device_mapping(L):
 
 def test_workspace_size(L):
     import tiled_top_sparse_gb300 as tts
-    assert L.tts_attn_workspace_bytes(256, 256, 1, 1, 64, tts.TTS_BF16) == 0
+    # bf16 inputs: only the work-item counter of the persistent kernel
+    assert L.tts_attn_workspace_bytes(256, 256, 1, 1, 64, tts.TTS_BF16) == 256
     n = L.tts_attn_workspace_bytes(256, 256, 1, 1, 64, tts.TTS_F32)
-    assert n >= 3 * 256 * 64 * 2
+    assert n >= 256 + 3 * 256 * 64 * 2
 
 
 # Fake, never-dereferenced pointers: host validation must reject before any CUDA call.
@@ -88,6 +89,8 @@ def test_attn_host_validation(L):
     assert _attn(L, d=96) == tts.TTS_ERR_UNSUPPORTED
     assert _attn(L, q=ctypes.c_void_p(0x1008)) == tts.TTS_ERR_INVALID_ARG  # misaligned
     assert _attn(L, dt=1) == tts.TTS_ERR_WORKSPACE  # fp32 needs a workspace
+    assert _attn(L, dt=0) == tts.TTS_ERR_WORKSPACE  # so does bf16 (the work counter)
+    assert _attn(L, ws=P, wsb=255) == tts.TTS_ERR_WORKSPACE
     assert _attn(L, tq=0) == tts.TTS_OK
 
 

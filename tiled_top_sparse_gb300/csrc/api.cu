@@ -59,6 +59,7 @@ inline tts_status from_cuda(cudaError_t e) {
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t kCounterBytes = 256;  // attention workspace: work-item counter
 
 }  // namespace
 
@@ -88,12 +89,13 @@ int tts_version(void) { return 100; }
 
 size_t tts_attn_workspace_bytes(int64_t total_q, int64_t total_k, int32_t num_heads_q,
                                 int32_t num_heads_kv, int32_t head_dim, tts_dtype in_dtype) {
-  if (in_dtype != TTS_F32 || total_q < 0 || total_k < 0 || num_heads_q < 1 || num_heads_kv < 1 ||
-      head_dim < 1)
-    return 0;
+  if (total_q < 0 || total_k < 0 || num_heads_q < 1 || num_heads_kv < 1 || head_dim < 1) return 0;
+  // 256 bytes for the work-item counter of the persistent kernel, then (fp32 inputs)
+  // the bf16 copies of q, k and v.
+  if (in_dtype != TTS_F32) return kCounterBytes;
   const size_t nq = (size_t)total_q * num_heads_q * head_dim * 2;
   const size_t nk = (size_t)total_k * num_heads_kv * head_dim * 2;
-  return align_up(nq, 256) + 2 * align_up(nk, 256);
+  return kCounterBytes + align_up(nq, 256) + 2 * align_up(nk, 256);
 }
 
 tts_status tts_attn_fwd_varlen(const void* q, const void* k, const void* v, tts_dtype in_dtype,
@@ -120,16 +122,17 @@ tts_status tts_attn_fwd_varlen(const void* q, const void* k, const void* v, tts_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (total_q == 0 || max_seqlen_q == 0) return TTS_OK;  // nothing to compute
 
+  const size_t need =
+      tts_attn_workspace_bytes(total_q, total_k, num_heads_q, num_heads_kv, head_dim, in_dtype);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return TTS_ERR_WORKSPACE;
   AttnArgs a;
   a.q = q;
   a.k = k;
   a.v = v;
+  a.work_counter = static_cast<uint32_t*>(workspace);
   if (in_dtype == TTS_F32) {
-    const size_t need =
-        tts_attn_workspace_bytes(total_q, total_k, num_heads_q, num_heads_kv, head_dim, in_dtype);
-    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
-      return TTS_ERR_WORKSPACE;
-    uint8_t* w = static_cast<uint8_t*>(workspace);
+    uint8_t* w = static_cast<uint8_t*>(workspace) + kCounterBytes;
     const int64_t nq = total_q * num_heads_q * head_dim;
     const int64_t nk = total_k * num_heads_kv * head_dim;
     void* qb = w;

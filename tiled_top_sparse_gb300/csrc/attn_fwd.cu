@@ -9,8 +9,11 @@
 // as -inf (3.3), and the online-softmax merge of "推理引擎的蝴蝶效应" (进一步探索,
 // equations 1-2) applied tile after tile in a fixed order.
 //
-// How (one CTA = one (sequence, 256-row query pair, head)):
-//   warp 0        TMA producer: Q tiles once, then K/V 128-row tiles into a ring
+// How: one persistent CTA per SM takes work items -- (sequence, 256-row query
+// pair, head), heaviest first -- from a global counter in the caller's workspace:
+//   warp 0        TMA producer: picks the items, then per item K/V 128-row tiles
+//                 into a ring and the two Q tiles (the next item's loads overlap
+//                 the current item's last tiles and epilogue)
 //   warp 1        TMEM allocator + tcgen05 MMA issuer (the whole warp runs the
 //                 issue loop converged; one elected lane issues)
 //   warps 4..7    softmax warpgroup 0 (query rows 0..127 of the pair)
@@ -54,7 +57,9 @@ struct AttnCfg {
   static constexpr int kVTileBytes = kVBoxes * kVBoxBytes;
   static constexpr int kPvN = kTail ? 96 : D;
   static constexpr int kStages = (D <= 80) ? 3 : 2;
-  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + kStages * kVTileBytes + 1024;
+  static constexpr int kStageBytes = 8 * 4096;  // output staging, 4 KB per softmax warp
+  static constexpr int kSmemBytes =
+      (2 + kStages) * kTileBytes + kStages * kVTileBytes + kStageBytes + 1024;
   static_assert(kTail == 0 || kTail == 16, "head_dim must be 64, 80 or 128");
 };
 
@@ -67,6 +72,8 @@ struct AttnMaps {
 struct AttnParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
+  uint32_t* work_counter;  // items handed out so far (zeroed before the launch)
+  int n_items;
   float* out;
   float* lse;
   uint32_t* dev_status;
@@ -120,6 +127,52 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
 }
 
 
+// One work item = (256-row query pair, sequence, head); `it` enumerates them with
+// the heaviest (latest, causal) pairs of every sequence first. Every role decodes
+// an item the same way. Returns false for items with nothing to compute and for
+// sequences whose cu_seqlens entries are invalid.
+struct Item {
+  int64_t q_start, k_start, Lq, Lk, q_lo;
+  int h, g, n_tiles;
+};
+__device__ __forceinline__ bool decode_item(const AttnParams& p, int it, Item& w, bool* bad) {
+  const int h = it % p.hq;
+  const int t = it / p.hq;
+  const int b = t % p.batch;
+  const int pr = p.pairs_max - 1 - t / p.batch;
+  const int64_t q_start = p.cu_q[b], k_start = p.cu_k[b];
+  const int64_t q_end = p.cu_q[b + 1], k_end = p.cu_k[b + 1];
+  const int64_t Lq = q_end - q_start, Lk = k_end - k_start;
+  *bad = false;
+  if (q_start < 0 || k_start < 0 || Lq < 0 || Lk < 0 || q_end > p.total_q || k_end > p.total_k ||
+      Lq > p.max_seqlen_q || Lk > p.max_seqlen_k) {
+    *bad = (pr == 0 && h == 0);  // report each bad sequence once
+    return false;
+  }
+  const int64_t q_lo = (int64_t)pr * 2 * kBlockM;  // first query row (within the sequence)
+  if (q_lo >= Lq) return false;
+  int64_t kv_end = Lk;
+  if (p.causal) {
+    const int64_t i_last = (q_lo + 2 * kBlockM < Lq ? q_lo + 2 * kBlockM : Lq) - 1;
+    const int64_t lim = i_last + (Lk - Lq) + 1;
+    kv_end = lim < kv_end ? lim : kv_end;
+    if (kv_end < 0) kv_end = 0;
+  }
+  w.q_start = q_start;
+  w.k_start = k_start;
+  w.Lq = Lq;
+  w.Lk = Lk;
+  w.q_lo = q_lo;
+  w.h = h;
+  w.g = h / (p.hq / p.hkv);
+  w.n_tiles = (int)((kv_end + kBlockN - 1) / kBlockN);
+  return true;
+}
+
+// Persistent: one CTA per SM takes items from a global counter until none are left.
+// Per CTA, items flow through a two-slot ring (producer -> MMA warp + softmax warps);
+// barrier phases run on counters that continue across items: gt = K/V tiles so far
+// (ring slots, S / P phases), nq = items with at least one tile (Q, O phases).
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p) {
@@ -133,39 +186,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // as soon as both S MMAs of its tile are done, a PV pair before V's slot
   // (bar_kv_empty), so the next K load starts that much earlier.
   constexpr bool kOneKV = NS >= 3;
-  __shared__ __align__(8) uint64_t bar_q, bar_k[NS], bar_v[NS], bar_k_empty[NS],
-      bar_kv_empty[NS], bar_s[2], bar_p[2], bar_o[2], bar_drain;
+  __shared__ __align__(8) uint64_t bar_item_full[2], bar_item_empty[2], bar_q[2], bar_q_empty[2],
+      bar_k[NS], bar_v[NS], bar_k_empty[NS], bar_kv_empty[NS], bar_s[2], bar_p[2], bar_o[2],
+      bar_drain;
+  __shared__ int s_item[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- work item: heavy (late, causal) pairs of every sequence first ----
-  const int lin = blockIdx.x;
-  const int h = lin % p.hq;
-  const int t = lin / p.hq;
-  const int b = t % p.batch;
-  const int pr = p.pairs_max - 1 - t / p.batch;
-  const int64_t q_start = p.cu_q[b], k_start = p.cu_k[b];
-  const int64_t q_end = p.cu_q[b + 1], k_end = p.cu_k[b + 1];
-  const int64_t Lq = q_end - q_start, Lk = k_end - k_start;
-  if (q_start < 0 || k_start < 0 || Lq < 0 || Lk < 0 || q_end > p.total_q || k_end > p.total_k ||
-      Lq > p.max_seqlen_q || Lk > p.max_seqlen_k) {
-    if (tid == 0 && pr == 0 && h == 0 && p.dev_status) atomicOr(p.dev_status, kDevBadArg);
-    return;
-  }
-  const int64_t q_lo = (int64_t)pr * 2 * kBlockM;  // first query row (within the sequence)
-  if (q_lo >= Lq) return;
-  const int g = h / (p.hq / p.hkv);
-  int64_t kv_end = Lk;
-  if (p.causal) {
-    const int64_t i_last = (q_lo + 2 * kBlockM < Lq ? q_lo + 2 * kBlockM : Lq) - 1;
-    const int64_t lim = i_last + (Lk - Lq) + 1;
-    kv_end = lim < kv_end ? lim : kv_end;
-    if (kv_end < 0) kv_end = 0;
-  }
-  const int n_tiles = (int)((kv_end + kBlockN - 1) / kBlockN);
-
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t s_base = smem_u32(smem);
@@ -174,20 +202,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto sV = [&](int st) {
     return s_base + (2 + NS) * C::kTileBytes + st * C::kVTileBytes;
   };
+  // Output staging: 4 KB per softmax warp, after the K/V ring.
+  uint8_t* stage_base = smem + (2 + NS) * C::kTileBytes + NS * C::kVTileBytes;
 
   if (tid == 0) {
     s_abort = 0;
-    mbar_init(smem_u32(&bar_q), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_item_full[i]), 1);
+      mbar_init(smem_u32(&bar_item_empty[i]), 1 + 8);  // MMA warp + 8 softmax warps
+      mbar_init(smem_u32(&bar_q[i]), 1);
+      mbar_init(smem_u32(&bar_q_empty[i]), 1);
+      mbar_init(smem_u32(&bar_s[i]), 1);
+      mbar_init(smem_u32(&bar_p[i]), kBlockM);
+      mbar_init(smem_u32(&bar_o[i]), 1);
+    }
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bar_k[i]), 1);
       mbar_init(smem_u32(&bar_v[i]), 1);
       mbar_init(smem_u32(&bar_k_empty[i]), 1);
       mbar_init(smem_u32(&bar_kv_empty[i]), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_s[i]), 1);
-      mbar_init(smem_u32(&bar_p[i]), kBlockM);
-      mbar_init(smem_u32(&bar_o[i]), 1);
     }
     mbar_init(smem_u32(&bar_drain), 1);
     fence_mbar_init();
@@ -201,106 +234,195 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
+  volatile int* item_slot = s_item;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
       prefetch_tmap(&maps.v);
-      const uint32_t bq = smem_u32(&bar_q);
-      if (n_tiles > 0) {
-        mbar_arrive_expect_tx(bq, 2 * C::kTileBytes);
-        for (int w = 0; w < 2; ++w)
-          load_tile<D>(sQ[w], &maps.q, &maps.q_t, bq, h, (int)(q_start + q_lo + w * kBlockM));
-      }
-      int issued = 0, issued_v = 0;  // tiles whose K / V copies were started
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % NS;
-        const uint32_t empty_ph = ((j / NS) - 1) & 1;
-        if (j >= NS && !mbar_wait(smem_u32(kOneKV ? &bar_kv_empty[st] : &bar_k_empty[st]),
-                                  empty_ph, abort_flag, p.dev_status))
-          break;
-        const int tok = (int)(k_start + (int64_t)j * kBlockN);
+      int ni = 0, nq = 0, gt = 0;
+      int last_k[NS], last_v[NS];  // latest tile armed on each ring slot (-1: none)
+      for (int i = 0; i < NS; ++i) last_k[i] = last_v[i] = -1;
+      int q_armed[2] = {0, 0};  // per Q tile: items whose Q copy was started
+      // Start the K (and V) copies of ring tile gj = item tile j.
+      auto load_k = [&](int gj, const Item& w, int j) -> bool {
+        const int st = gj % NS;
+        const uint32_t empty_ph = ((gj / NS) - 1) & 1;
+        if (gj >= NS && !mbar_wait(smem_u32(kOneKV ? &bar_kv_empty[st] : &bar_k_empty[st]),
+                                   empty_ph, abort_flag, p.dev_status))
+          return false;
+        const int tok = (int)(w.k_start + (int64_t)j * kBlockN);
         const uint32_t bk = smem_u32(&bar_k[st]);
-        const uint32_t bv = kOneKV ? bk : smem_u32(&bar_v[st]);
         mbar_arrive_expect_tx(bk, kOneKV ? C::kTileBytes + C::kVTileBytes : C::kTileBytes);
-        load_tile<D>(sK(st), &maps.k, &maps.k_t, bk, g, tok);
+        load_tile<D>(sK(st), &maps.k, &maps.k_t, bk, w.g, tok);
+        last_k[st] = gj;
+        return true;
+      };
+      auto load_v = [&](int gj, const Item& w, int j) -> bool {
+        const int st = gj % NS;
+        const uint32_t bv = smem_u32(kOneKV ? &bar_k[st] : &bar_v[st]);
         if (!kOneKV) {
-          issued = j + 1;  // K of this tile is in flight
-          if (j >= NS &&
-              !mbar_wait(smem_u32(&bar_kv_empty[st]), empty_ph, abort_flag, p.dev_status))
-            break;
+          if (gj >= NS && !mbar_wait(smem_u32(&bar_kv_empty[st]), ((gj / NS) - 1) & 1, abort_flag,
+                                     p.dev_status))
+            return false;
           mbar_arrive_expect_tx(bv, C::kVTileBytes);
         }
+        const int tok = (int)(w.k_start + (int64_t)j * kBlockN);
         if constexpr (C::kTail != 0) {
 #pragma unroll
           for (int b = 0; b < C::kVBoxes; ++b)
-            tma_load_3d(sV(st) + b * C::kVBoxBytes, &maps.v_t, bv, b * 32, g, tok);
+            tma_load_3d(sV(st) + b * C::kVBoxBytes, &maps.v_t, bv, b * 32, w.g, tok);
         } else {
-          load_tile<D>(sV(st), &maps.v, &maps.v, bv, g, tok);
+          load_tile<D>(sV(st), &maps.v, &maps.v, bv, w.g, tok);
         }
-        issued = issued_v = j + 1;
+        last_v[st] = gj;
+        return true;
+      };
+      bool ok = true;
+      while (ok) {
+        Item w;
+        int it;
+        for (;;) {  // next item with work (bad sequences are reported here, once)
+          it = (int)atomicAdd(p.work_counter, 1u);
+          if (it >= p.n_items) {
+            it = -1;
+            break;
+          }
+          bool bad;
+          if (decode_item(p, it, w, &bad)) break;
+          if (bad && p.dev_status) atomicOr(p.dev_status, kDevBadArg);
+        }
+        const int slot = ni & 1;
+        if (ni >= 2 &&
+            !mbar_wait(smem_u32(&bar_item_empty[slot]), ((ni >> 1) - 1) & 1, abort_flag,
+                       p.dev_status))
+          break;
+        item_slot[slot] = it;
+        mbar_arrive(smem_u32(&bar_item_full[slot]));  // release: the slot write is visible
+        ++ni;
+        if (it < 0) break;
+        const int n = w.n_tiles;
+        if (n == 0) continue;
+        // The first ring tiles go first (their slots free up while the previous item
+        // finishes); Q waits for the previous item's last S MMAs; the remaining tiles
+        // need slots that this item's own MMAs free, so they come after Q.
+        const int pre = n < NS ? n : NS;
+        for (int j = 0; ok && j < pre; ++j) ok = load_k(gt + j, w, j) && load_v(gt + j, w, j);
+        for (int wq = 0; ok && wq < 2; ++wq) {
+          if (nq >= 1 && !mbar_wait(smem_u32(&bar_q_empty[wq]), (nq - 1) & 1, abort_flag,
+                                    p.dev_status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bq = smem_u32(&bar_q[wq]);
+          mbar_arrive_expect_tx(bq, C::kTileBytes);
+          load_tile<D>(sQ[wq], &maps.q, &maps.q_t, bq, w.h,
+                       (int)(w.q_start + w.q_lo + wq * kBlockM));
+          q_armed[wq] = nq + 1;
+        }
+        for (int j = pre; ok && j < n; ++j) ok = load_k(gt + j, w, j) && load_v(gt + j, w, j);
+        gt += n;
+        ++nq;
       }
-      if (*abort_flag && n_tiles > 0) {
-        // Best-effort drain of copies still in flight before the CTA can exit.
-        mbar_wait(bq, 0, nullptr, nullptr);
-        for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j) {
-          mbar_wait(smem_u32(&bar_k[j % NS]), (j / NS) & 1, nullptr, nullptr);
-          if (!kOneKV && j < issued_v)
-            mbar_wait(smem_u32(&bar_v[j % NS]), (j / NS) & 1, nullptr, nullptr);
+      if (*abort_flag) {
+        // Best-effort drain of copies still in flight before the CTA can exit: each
+        // barrier's latest armed phase is the only one that can still be pending.
+        for (int wq = 0; wq < 2; ++wq)
+          if (q_armed[wq] > 0)
+            mbar_wait(smem_u32(&bar_q[wq]), (q_armed[wq] - 1) & 1, nullptr, nullptr);
+        for (int st = 0; st < NS; ++st) {
+          if (last_k[st] >= 0)
+            mbar_wait(smem_u32(&bar_k[st]), (last_k[st] / NS) & 1, nullptr, nullptr);
+          if (!kOneKV && last_v[st] >= 0)
+            mbar_wait(smem_u32(&bar_v[st]), (last_v[st] / NS) & 1, nullptr, nullptr);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (n_tiles > 0) {
-      const uint32_t e = elect_one();
-      const uint32_t S_t[2] = {tmem, tmem + 128};
-      const uint32_t O_t[2] = {tmem + 256, tmem + 384};
-      constexpr uint32_t kTailOff = C::kMainBoxes * C::kBoxBytes;
-      uint64_t qd[2], qtd[2], kd[NS], ktd[NS], vd[NS];
-      for (int w = 0; w < 2; ++w) {
-        qd[w] = smem_desc(sQ[w], 16, 1024, kSw128);
-        qtd[w] = smem_desc(sQ[w] + kTailOff, 16, 256, kSw32);
-      }
-      for (int i = 0; i < NS; ++i) {
-        kd[i] = smem_desc(sK(i), 16, 1024, kSw128);
-        ktd[i] = smem_desc(sK(i) + kTailOff, 16, 256, kSw32);
-        vd[i] = C::kTail ? smem_desc(sV(i), C::kVBoxBytes, 512, kSw64)
-                         : smem_desc(sV(i), C::kBoxBytes, 1024, kSw128);
-      }
-      bool ok = warp_wait(smem_u32(&bar_q), 0, abort_flag, p.dev_status) &&
-                warp_wait(smem_u32(&bar_k[0]), 0, abort_flag, p.dev_status);
-      if (ok) {
-        tc_fence_after();
-        issue_qk<D>(S_t[0], qd[0], kd[0], qtd[0], ktd[0], e);
-        mma_commit_elect(smem_u32(&bar_s[0]), e);
-        issue_qk<D>(S_t[1], qd[1], kd[0], qtd[1], ktd[0], e);
-        mma_commit_elect(smem_u32(&bar_s[1]), e);
-        if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[0]), e);
-      }
+    const uint32_t e = elect_one();
+    const uint32_t S_t[2] = {tmem, tmem + 128};
+    const uint32_t O_t[2] = {tmem + 256, tmem + 384};
+    constexpr uint32_t kTailOff = C::kMainBoxes * C::kBoxBytes;
+    uint64_t qd[2], qtd[2], kd[NS], ktd[NS], vd[NS];
+    for (int w = 0; w < 2; ++w) {
+      qd[w] = smem_desc(sQ[w], 16, 1024, kSw128);
+      qtd[w] = smem_desc(sQ[w] + kTailOff, 16, 256, kSw32);
+    }
+    for (int i = 0; i < NS; ++i) {
+      kd[i] = smem_desc(sK(i), 16, 1024, kSw128);
+      ktd[i] = smem_desc(sK(i) + kTailOff, 16, 256, kSw32);
+      vd[i] = C::kTail ? smem_desc(sV(i), C::kVBoxBytes, 512, kSw64)
+                       : smem_desc(sV(i), C::kBoxBytes, 1024, kSw128);
+    }
+    int ni = 0, nq = 0, gt = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = ni & 1;
+      if (!warp_wait(smem_u32(&bar_item_full[slot]), (ni >> 1) & 1, abort_flag, p.dev_status))
+        break;
+      const int it = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_item_empty[slot]));
+      ++ni;
+      if (it < 0) break;
+      Item w;
+      bool bad;
+      decode_item(p, it, w, &bad);
+      const int n = w.n_tiles;
+      if (n == 0) continue;
+      const int st0 = gt % NS;
+      ok = warp_wait(smem_u32(&bar_q[0]), nq & 1, abort_flag, p.dev_status) &&
+           warp_wait(smem_u32(&bar_k[st0]), (gt / NS) & 1, abort_flag, p.dev_status);
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk<D>(S_t[0], qd[0], kd[st0], qtd[0], ktd[st0], e);
+      mma_commit_elect(smem_u32(&bar_s[0]), e);
+      if (n == 1) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
+      ok = warp_wait(smem_u32(&bar_q[1]), nq & 1, abort_flag, p.dev_status);
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk<D>(S_t[1], qd[1], kd[st0], qtd[1], ktd[st0], e);
+      mma_commit_elect(smem_u32(&bar_s[1]), e);
+      if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st0]), e);
+      if (n == 1) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
       // Order on the tensor core: PV0(j) S0(j+1) PV1(j) S1(j+1).
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % NS;
-        const bool more = j + 1 < n_tiles;
-        const int st1 = (j + 1) % NS;
-        if (!kOneKV && !warp_wait(smem_u32(&bar_v[st]), (j / NS) & 1, abort_flag, p.dev_status))
+      for (int j = 0; j < n; ++j) {
+        const int gj = gt + j;
+        const int st = gj % NS;
+        const bool more = j + 1 < n;
+        const int st1 = (gj + 1) % NS;
+        const bool last_s = j + 2 == n;  // S(j+1) is this item's last S MMA
+        if (!kOneKV && !warp_wait(smem_u32(&bar_v[st]), (gj / NS) & 1, abort_flag, p.dev_status)) {
+          ok = false;
           break;
+        }
         // warpgroup 0
-        if (!warp_wait(smem_u32(&bar_p[0]), j & 1, abort_flag, p.dev_status)) break;
+        if (!warp_wait(smem_u32(&bar_p[0]), gj & 1, abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         issue_pv<D>(O_t[0], S_t[0], vd[st], j > 0, e);
         if (more) {
-          if (!warp_wait(smem_u32(&bar_k[st1]), ((j + 1) / NS) & 1, abort_flag, p.dev_status))
+          if (!warp_wait(smem_u32(&bar_k[st1]), ((gj + 1) / NS) & 1, abort_flag, p.dev_status)) {
+            ok = false;
             break;
+          }
           tc_fence_after();
           issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
           mma_commit_elect(smem_u32(&bar_s[0]), e);
+          if (last_s) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
         } else {
           mma_commit_elect(smem_u32(&bar_o[0]), e);
         }
         // warpgroup 1
-        if (!warp_wait(smem_u32(&bar_p[1]), j & 1, abort_flag, p.dev_status)) break;
+        if (!warp_wait(smem_u32(&bar_p[1]), gj & 1, abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         issue_pv<D>(O_t[1], S_t[1], vd[st], j > 0, e);
         mma_commit_elect(smem_u32(&bar_kv_empty[st]), e);
@@ -308,102 +430,122 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
           mma_commit_elect(smem_u32(&bar_s[1]), e);
           if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
+          if (last_s) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
         } else {
           mma_commit_elect(smem_u32(&bar_o[1]), e);
         }
       }
-      // Drain: every MMA issued by this warp is complete before TMEM is freed.
-      mma_commit_elect(smem_u32(&bar_drain), e);
-      mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
+      gt += n;
+      ++nq;
     }
+    // Drain: every MMA issued by this warp is complete before TMEM is freed.
+    mma_commit_elect(smem_u32(&bar_drain), e);
+    mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int wg = (warp - 4) >> 2;         // 0 or 1
+    const int wg = (warp - 4) >> 2;            // 0 or 1
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane == row within the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t S_row = tmem + wg * 128 + lane_off;
     const uint32_t O_row = tmem + 256 + wg * 128 + lane_off;
-    const int64_t i = q_lo + wg * kBlockM + row;  // query row within the sequence
-    int64_t limit = Lk;                          // keys [0, limit) visible to this row
-    if (p.causal) {
-      const int64_t lim = i + (Lk - Lq) + 1;
-      limit = lim < limit ? lim : limit;
-    }
+    float4* stage = reinterpret_cast<float4*>(stage_base + (warp - 4) * 4096);
     const float c = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    int ni = 0, nq = 0, gt = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      // tcgen05.ld/st are warp-collective: leave the loop as a whole warp.
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_s[wg]), j & 1, abort_flag,
-                                              p.dev_status));
+    while (ok) {
+      const int slot = ni & 1;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_item_full[slot]), (ni >> 1) & 1,
+                                              abort_flag, p.dev_status));
+      if (!ok) break;
+      const int it = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_item_empty[slot]));
+      ++ni;
+      if (it < 0) break;
+      Item w;
+      bool bad;
+      decode_item(p, it, w, &bad);
+      const int n_tiles = w.n_tiles;
+      const int64_t Lq = w.Lq, Lk = w.Lk;
+      const int64_t i = w.q_lo + wg * kBlockM + row;  // query row within the sequence
+      int64_t limit = Lk;                            // keys [0, limit) visible to this row
+      if (p.causal) {
+        const int64_t lim = i + (Lk - Lq) + 1;
+        limit = lim < limit ? lim : limit;
+      }
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int gj = gt + j;
+        // tcgen05.ld/st are warp-collective: leave the loop as a whole warp.
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_s[wg]), gj & 1, abort_flag,
+                                                p.dev_status));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        float part_max[4];  // TMEM returns each 32-column chunk's max with the data
+  #pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          part_max[q4] =
+              tmem_ld32_max(S_row + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
+        tmem_ld_wait();
+        float* s = reinterpret_cast<float*>(sr);
+        const int64_t kv0 = (int64_t)j * kBlockN;
+        float tile_max = fmaxf(fmax3(part_max[0], part_max[1], part_max[2]), part_max[3]);
+        if (kv0 + kBlockN > limit) {  // masked columns must not count in the max
+          const int64_t lim = limit - kv0;
+  #pragma unroll
+          for (int cc = 0; cc < 128; ++cc)
+            if (cc >= lim) s[cc] = -INFINITY;
+          tile_max = row_max<128>(s);
+        }
+        const float m_new = fmaxf(m_ref, tile_max);
+        const bool resc = (m_new - m_ref) * c > 8.0f;  // false for -inf - -inf (NaN)
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2_approx((m_ref - m_new) * c);  // 0 when m_ref = -inf
+          l *= alpha;
+          m_ref = m_new;
+        }
+        const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
+        // P packed as bf16 pairs over sr[0..63], in place.
+        l += exp2_pack_sum<128>(sr, c, neg_mc);
+  #pragma unroll
+        for (int q4 = 0; q4 < 2; ++q4)
+          tmem_st32(S_row + q4 * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[q4 * 32]));
+        // Rescale O (its previous PV finished: it was issued before this tile's S MMA,
+        // whose completion this thread observed).
+        if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+  #pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(O_row + c0, o);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(O_row + c0, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p[wg]));
+      }
+      // ---- epilogue: out = O / l, lse = m * scale + ln l ----
+      if (ok && n_tiles > 0)
+        ok = __all_sync(0xFFFFFFFFu,
+                        mbar_wait(smem_u32(&bar_o[wg]), nq & 1, abort_flag, p.dev_status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[128];
-      float part_max[4];  // TMEM returns each 32-column chunk's max with the data
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        part_max[q4] =
-            tmem_ld32_max(S_row + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
-      tmem_ld_wait();
-      float* s = reinterpret_cast<float*>(sr);
-      const int64_t kv0 = (int64_t)j * kBlockN;
-      float tile_max = fmaxf(fmax3(part_max[0], part_max[1], part_max[2]), part_max[3]);
-      if (kv0 + kBlockN > limit) {  // masked columns must not count in the max
-        const int64_t lim = limit - kv0;
-#pragma unroll
-        for (int cc = 0; cc < 128; ++cc)
-          if (cc >= lim) s[cc] = -INFINITY;
-        tile_max = row_max<128>(s);
-      }
-      const float m_new = fmaxf(m_ref, tile_max);
-      const bool resc = (m_new - m_ref) * c > 8.0f;  // false for -inf - -inf (NaN)
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2_approx((m_ref - m_new) * c);  // 0 when m_ref = -inf
-        l *= alpha;
-        m_ref = m_new;
-      }
-      const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
-      // P packed as bf16 pairs over sr[0..63], in place.
-      l += exp2_pack_sum<128>(sr, c, neg_mc);
-#pragma unroll
-      for (int q4 = 0; q4 < 2; ++q4)
-        tmem_st32(S_row + q4 * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[q4 * 32]));
-      // Rescale O (its previous PV finished: it was issued before this tile's S MMA,
-      // whose completion this thread observed).
-      if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld16(O_row + c0, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st16(O_row + c0, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p[wg]));
-    }
-    // ---- epilogue: out = O / l, lse = m * scale + ln l ----
-    if (ok && n_tiles > 0)
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_o[wg]), 0, abort_flag, p.dev_status));
-    tc_fence_after();
-    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    if (ok) {
-      // Rows leave TMEM one per thread; a 4 KB slice of this warpgroup's Q tile (no
-      // MMA reads it any more: bar_o covers every MMA issued for this tile) turns them
-      // into whole 128-byte row segments, so each store instruction writes full lines.
-      float4* stage = reinterpret_cast<float4*>(smem + wg * C::kTileBytes + (warp & 3) * 4096);
-      const int64_t row0 = q_lo + wg * kBlockM + (warp & 3) * 32;  // this warp's first row
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      // Rows leave TMEM one per thread; this warp's 4 KB staging slice turns them into
+      // whole 128-byte row segments, so each store instruction writes full lines.
+      const int64_t row0 = w.q_lo + wg * kBlockM + (warp & 3) * 32;  // this warp's first row
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         constexpr int kW = 32;
-        const int w = (D - c0 < kW) ? D - c0 : kW;  // 32, or 16 for the d = 80 tail
+        const int cw = (D - c0 < kW) ? D - c0 : kW;  // 32, or 16 for the d = 80 tail
         uint32_t o[32];
         if (n_tiles > 0) {
-          if (w == 32) {
+          if (cw == 32) {
             tmem_ld32(O_row + c0, o);
           } else {
             tmem_ld16(O_row + c0, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
@@ -411,32 +553,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
+          for (int q = 0; q < 32; ++q) o[q] = 0u;
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          if (q < w / 4)
-            stage[lane * 8 + (q ^ (lane & 7))] =
-                make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                            __uint_as_float(o[4 * q + 2]) * inv_l,
-                            __uint_as_float(o[4 * q + 3]) * inv_l);
+          if (q < cw / 4)
+            stage[lane * 8 + (q ^ (lane & 7))] = make_float4(
+                __uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
         __syncwarp();
-        const int lpr = w / 4;  // lanes per row segment
+        const int lpr = cw / 4;  // lanes per row segment
         for (int rr = 0; rr < 32; rr += 32 / lpr) {
           const int r = rr + lane / lpr, q = lane % lpr;
           const float4 v = stage[r * 8 + (q ^ (r & 7))];
           const int64_t ii = row0 + r;
           if (ii < Lq)
-            *reinterpret_cast<float4*>(p.out + ((q_start + ii) * p.hq + h) * (int64_t)D + c0 +
-                                       4 * q) = v;
+            *reinterpret_cast<float4*>(p.out + ((w.q_start + ii) * p.hq + w.h) * (int64_t)D +
+                                       c0 + 4 * q) = v;
         }
         __syncwarp();
       }
+      if (i < Lq && p.lse != nullptr)
+        p.lse[(w.q_start + i) * p.hq + w.h] =
+            (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
+      gt += n_tiles;
+      if (n_tiles > 0) ++nq;
     }
-    const bool store = ok && i < Lq;
-    if (store && p.lse != nullptr)
-      p.lse[(q_start + i) * p.hq + h] =
-          (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
   }
 
   tc_fence_before();
@@ -505,13 +647,23 @@ cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
   p.pairs_max = (a.max_seqlen_q + 2 * kBlockM - 1) / (2 * kBlockM);
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  const int64_t grid = (int64_t)a.batch * p.pairs_max * a.hq;
-  if (grid == 0) return cudaSuccess;
-  if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int64_t items = (int64_t)a.batch * p.pairs_max * a.hq;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x7FFFFFFF || a.work_counter == nullptr) return cudaErrorInvalidConfiguration;
+  p.work_counter = a.work_counter;
+  p.n_items = (int)items;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // One persistent CTA per SM (the kernel's shared memory and TMEM allow one).
+  const int grid = (int)(items < sms ? items : sms);
+  e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D><<<(unsigned)grid, kAttnThreads, C::kSmemBytes, stream>>>(maps, p);
+  e = cudaMemsetAsync(a.work_counter, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<D><<<grid, kAttnThreads, C::kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
 }
 

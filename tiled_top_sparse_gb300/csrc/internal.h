@@ -26,6 +26,7 @@ struct AttnArgs {
   float* out;
   float* lse;
   uint32_t* dev_status;
+  uint32_t* work_counter;  // device scratch word (the launch zeroes it on the stream)
 };
 // Returns cudaSuccess or the first error; *drv_err receives a CUresult from tensor-map encoding.
 cudaError_t launch_attn_fwd(const AttnArgs& a, int* drv_err, cudaStream_t stream);
