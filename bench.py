@@ -197,6 +197,14 @@ class Step:
         self.o_sp = torch.empty((self.sp.q.shape[0], self.sp.q.shape[1], self.sp.dv), **f32)
         self.l_sp = torch.empty(self.sp.q.shape[:2], **f32)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # attention workspace (work-item counter), shared by the two stream-ordered calls
+        ws = max(tts.attn_workspace_bytes(self.vis.q.shape[0], self.vis.k.shape[0],
+                                          self.vis.q.shape[1], self.vis.k.shape[1],
+                                          self.vis.q.shape[2], torch.bfloat16),
+                 tts.attn_workspace_bytes(self.var.q.shape[0], self.var.k.shape[0],
+                                          self.var.q.shape[1], self.var.k.shape[1],
+                                          self.var.q.shape[2], torch.bfloat16))
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.flops = {"vision": self.vis.flops(), "varlen": self.var.flops(),
                       "sparse": self.sp.flops()}
         self.topk_bytes = self.tk.bytes()
@@ -214,12 +222,12 @@ class Step:
             q, k, v, cq, ck = self.d_vis
             t.attn_fwd_varlen(q, k, v, cq, ck, self.vis.max_seqlen_q, self.vis.max_seqlen_k,
                               False, self.vis.scale, out=self.o_vis, lse=self.l_vis,
-                              status=self.status)
+                              workspace=self.ws, status=self.status)
         elif name == "varlen":
             q, k, v, cq, ck = self.d_var
             t.attn_fwd_varlen(q, k, v, cq, ck, self.var.max_seqlen_q, self.var.max_seqlen_k,
                               True, self.var.scale, out=self.o_var, lse=self.l_var,
-                              status=self.status)
+                              workspace=self.ws, status=self.status)
         elif name == "topk":
             lg, rs, rl = self.d_tk
             t.topk_select(lg, rs, rl, self.tk.k, idx=self.o_idx, status=self.status)
