@@ -5,7 +5,10 @@
 // the k window positions with the largest values, ordered by value descending
 // and, among equal values, by ascending position.
 //
-// Steps per row, all in shared memory:
+// Windows of up to 4096 values (the indexer's rows are 2590 long) are ranked by a
+// stable LSD radix sort of the whole window on the inverted key (4 passes of 8 bits;
+// stability keeps equal values in ascending position), and the first k positions are
+// the answer. Longer windows take the select-then-sort path:
 //  1. map each float of the window to an order-preserving 32-bit key
 //     (-0 folded onto +0, so equal floats get equal keys);
 //  2. MSB-first radix select over 4 x 8-bit digits finds the key T of rank k
@@ -27,6 +30,10 @@ namespace {
 
 constexpr int kTopkThreads = 512;
 constexpr int kWarps = kTopkThreads / 32;
+constexpr int kSortPerThread = 8;                          // values per thread, radix path
+constexpr int kSortMax = kTopkThreads * kSortPerThread;    // longest window it sorts
+// Shared memory of the radix path: two key/position buffers and per-warp digit counters.
+constexpr size_t kRadixSmem = 2 * kSortMax * (4 + 2) + kWarps * 256 * 4;
 
 __device__ __forceinline__ uint32_t ordered_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -62,6 +69,84 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
   return before + x - v;
 }
 
+// Stable LSD radix sort of a window of n <= kSortMax keys, descending (the sort runs
+// ascending on ~key), carrying 16-bit positions; writes the first k positions to out.
+// Element order inside a pass: warp w owns indices [w * 32E, (w + 1) * 32E), step s
+// of lane l holds index w * 32E + 32 s + l, so ranks computed warp by warp and step
+// by step preserve the input order of equal digits.
+__device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n, int k,
+                                          int32_t* __restrict__ out, uint8_t* smem) {
+  uint32_t* const key_buf = reinterpret_cast<uint32_t*>(smem);              // [2][kSortMax]
+  uint16_t* const pos_buf = reinterpret_cast<uint16_t*>(smem + 8 * kSortMax);  // [2][kSortMax]
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + 12 * kSortMax);  // [kWarps][256]
+  __shared__ uint32_t digit_base[256];
+  __shared__ int warp_tot[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = (n + kTopkThreads - 1) / kTopkThreads;  // steps per warp (<= 8)
+  const int wbase = warp * 32 * E;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t* wcnt = cnt + warp * 256;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int in = pass & 1;
+    const int shift = 8 * pass;
+    for (int d = lane; d < 256; d += 32) wcnt[d] = 0u;
+    __syncwarp();
+    uint32_t key[kSortPerThread], dig[kSortPerThread], rank[kSortPerThread];
+    uint16_t pos[kSortPerThread];
+#pragma unroll
+    for (int st = 0; st < kSortPerThread; ++st) {
+      if (st < E) {
+        const int idx = wbase + 32 * st + lane;
+        const bool present = idx < n;
+        if (present) {
+          if (pass == 0) {
+            key[st] = ~ordered_key(__ldg(src + idx));
+            pos[st] = static_cast<uint16_t>(idx);
+          } else {
+            key[st] = key_buf[in * kSortMax + idx];
+            pos[st] = pos_buf[in * kSortMax + idx];
+          }
+        }
+        dig[st] = present ? (key[st] >> shift) & 0xFFu : 256u;
+        const uint32_t act = __ballot_sync(0xFFFFFFFFu, present);
+        if (present) {
+          const uint32_t peers = __match_any_sync(act, dig[st]);
+          const uint32_t c0 = wcnt[dig[st]];
+          rank[st] = c0 + __popc(peers & lt_mask);
+          __syncwarp(act);
+          if ((__ffs(peers) - 1) == lane) wcnt[dig[st]] = c0 + __popc(peers);
+        }
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    // Per digit: exclusive prefix over warps (in place) and the digit's total.
+    uint32_t total = 0;
+    if (tid < 256) {
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t c = cnt[w * 256 + tid];
+        cnt[w * 256 + tid] = total;
+        total += c;
+      }
+    }
+    int all;
+    const int before = block_excl_scan(tid < 256 ? (int)total : 0, warp_tot, &all);
+    if (tid < 256) digit_base[tid] = (uint32_t)before;
+    __syncthreads();
+#pragma unroll
+    for (int st = 0; st < kSortPerThread; ++st) {
+      if (st < E && dig[st] < 256u) {
+        const uint32_t dst = digit_base[dig[st]] + wcnt[dig[st]] + rank[st];
+        key_buf[(in ^ 1) * kSortMax + dst] = key[st];
+        pos_buf[(in ^ 1) * kSortMax + dst] = pos[st];
+      }
+    }
+    __syncthreads();
+  }
+  // Four passes: the sorted data is back in buffer 0.
+  for (int j = tid; j < k; j += kTopkThreads) out[j] = (j < n) ? (int32_t)pos_buf[j] : -1;
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
     const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
     const int32_t* __restrict__ row_lens, int k, int sort_n, int32_t* __restrict__ idx,
@@ -85,6 +170,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
   }
   const int n = static_cast<int>(len);
   const float* src = logits + r * row_stride + st;
+  if (n <= kSortMax) {
+    radix_topk(src, n, k, out, smem);
+    return;
+  }
   for (int j = tid; j < n; j += kTopkThreads) keys[j] = ordered_key(__ldg(src + j));
   __syncthreads();
 
@@ -194,9 +283,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
 
 size_t topk_smem_bytes(int64_t row_stride, int k) {
   const int64_t cap = row_stride < k ? row_stride : k;
-  int sort_n = 1;
+  int sort_n = 2;
   while (sort_n < cap) sort_n <<= 1;
-  return 8 * (size_t)sort_n + 4 * (size_t)row_stride;
+  const size_t sel = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
+  return sel < kRadixSmem ? kRadixSmem : sel;
 }
 
 cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t rows,
@@ -205,7 +295,8 @@ cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t 
   const int64_t cap = row_stride < k ? row_stride : k;
   int sort_n = 2;
   while (sort_n < cap) sort_n <<= 1;
-  const size_t smem = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
+  size_t smem = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
+  if (smem < kRadixSmem) smem = kRadixSmem;
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
