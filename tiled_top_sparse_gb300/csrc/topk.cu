@@ -91,30 +91,33 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
     const int shift = 8 * pass;
     for (int d = lane; d < 256; d += 32) wcnt[d] = 0u;
     __syncwarp();
-    uint32_t key[kSortPerThread], dig[kSortPerThread], rank[kSortPerThread];
-    uint16_t pos[kSortPerThread];
+    // Per element: its key, and (position << 16 | rank within its digit and warp); the
+    // digit is recomputed from the key. Both fit 16 bits (n <= 4096).
+    uint32_t key[kSortPerThread], pr[kSortPerThread];
 #pragma unroll
     for (int st = 0; st < kSortPerThread; ++st) {
       if (st < E) {
         const int idx = wbase + 32 * st + lane;
         const bool present = idx < n;
+        uint32_t pos = 0;
         if (present) {
           if (pass == 0) {
             key[st] = ~ordered_key(__ldg(src + idx));
-            pos[st] = static_cast<uint16_t>(idx);
+            pos = static_cast<uint32_t>(idx);
           } else {
             key[st] = key_buf[in * kSortMax + idx];
-            pos[st] = pos_buf[in * kSortMax + idx];
+            pos = pos_buf[in * kSortMax + idx];
           }
         }
-        dig[st] = present ? (key[st] >> shift) & 0xFFu : 256u;
+        const uint32_t dig = (key[st] >> shift) & 0xFFu;
         const uint32_t act = __ballot_sync(0xFFFFFFFFu, present);
+        pr[st] = 0xFFFFFFFFu;  // absent
         if (present) {
-          const uint32_t peers = __match_any_sync(act, dig[st]);
-          const uint32_t c0 = wcnt[dig[st]];
-          rank[st] = c0 + __popc(peers & lt_mask);
+          const uint32_t peers = __match_any_sync(act, dig);
+          const uint32_t c0 = wcnt[dig];
+          pr[st] = (pos << 16) | (c0 + __popc(peers & lt_mask));
           __syncwarp(act);
-          if ((__ffs(peers) - 1) == lane) wcnt[dig[st]] = c0 + __popc(peers);
+          if ((__ffs(peers) - 1) == lane) wcnt[dig] = c0 + __popc(peers);
         }
         __syncwarp();
       }
@@ -135,10 +138,11 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
     __syncthreads();
 #pragma unroll
     for (int st = 0; st < kSortPerThread; ++st) {
-      if (st < E && dig[st] < 256u) {
-        const uint32_t dst = digit_base[dig[st]] + wcnt[dig[st]] + rank[st];
+      if (st < E && pr[st] != 0xFFFFFFFFu) {
+        const uint32_t dig = (key[st] >> shift) & 0xFFu;
+        const uint32_t dst = digit_base[dig] + wcnt[dig] + (pr[st] & 0xFFFFu);
         key_buf[(in ^ 1) * kSortMax + dst] = key[st];
-        pos_buf[(in ^ 1) * kSortMax + dst] = pos[st];
+        pos_buf[(in ^ 1) * kSortMax + dst] = static_cast<uint16_t>(pr[st] >> 16);
       }
     }
     __syncthreads();
@@ -147,7 +151,8 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
   for (int j = tid; j < k; j += kTopkThreads) out[j] = (j < n) ? (int32_t)pos_buf[j] : -1;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
+// Three CTAs per SM (<= 40 registers a thread): 456 resident rows on 152 SMs.
+__global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
     const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
     const int32_t* __restrict__ row_lens, int k, int sort_n, int32_t* __restrict__ idx,
     uint32_t* dev_status) {
