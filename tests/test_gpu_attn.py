@@ -146,3 +146,26 @@ def test_bad_cu_seqlens_flagged_not_faulting(tts):
                         inp.scale, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & tts.TTS_DEV_BAD_ARG
+
+
+def test_persistent_schedule_many_items_workspace_reuse(tts):
+    # 32 heads x 11 ragged sequences: ~500 work items on 152 persistent CTAs, items
+    # with no key tiles (causal, fewer keys than queries), empty sequences, one workspace
+    # reused by consecutive calls (its counter is re-zeroed on the stream by each call).
+    inp = W.dense_inputs([0, 1, 700, 2, 0, 900, 3, 129, 257, 64, 1],
+                         [0, 1, 700, 2, 5, 900, 1, 129, 257, 64, 0],
+                         hq=32, hkv=8, d=128, causal=True, seed=43)
+    dev = torch.device("cuda")
+    args = [t.to(dev) for t in (inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k)]
+    ws = torch.empty(tts.attn_workspace_bytes(inp.q.shape[0], inp.k.shape[0], 32, 8, 128,
+                                              torch.bfloat16), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = [tts.attn_fwd_varlen(*args, inp.max_seqlen_q, inp.max_seqlen_k, True, inp.scale,
+                                workspace=ws, status=st) for _ in range(3)]
+    tts.check_status(st)
+    ref_o, ref_l = oracle_full(inp)
+    assert_close_attn(outs[0][0].cpu().numpy(), ref_o, "persistent many items")
+    assert_lse_close(outs[0][1].cpu().numpy(), ref_l, "persistent many items")
+    for o, l in outs[1:]:  # the item-to-CTA assignment varies; the results may not
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
