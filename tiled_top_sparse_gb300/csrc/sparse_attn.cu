@@ -399,24 +399,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n_tiles > 0)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_o), 0, abort_flag, p.dev_status));
     tc_fence_after();
-    float* orow = p.out + ((int64_t)n * kHeads + h) * kDv + 256 * r;
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    if (ok && n_tiles > 0) {
+    if (ok) {
+      // Each thread holds one head's 256 values; a 4 KB slice of the (now idle) gather
+      // stage per warp turns them into 128-byte segments, four heads per store.
+      float4* stage = reinterpret_cast<float4*>(smem + kQhiBytes + (warp & 3) * 4096);
       const uint32_t O_row = tmem + 256 + lane_off;
+      float* obase = p.out + ((int64_t)n * kHeads + (warp & 3) * 32) * kDv + 256 * r;
 #pragma unroll 1
       for (int c0 = 0; c0 < 256; c0 += 32) {
         uint32_t o[32];
-        tmem_ld32(O_row + c0, o);
-        tmem_ld_wait();
+        if (n_tiles > 0) {
+          tmem_ld32(O_row + c0, o);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(orow + c0 + e) =
-              make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
-                          __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          stage[lane * 8 + (q ^ (lane & 7))] =
+              make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                          __uint_as_float(o[4 * q + 2]) * inv_l,
+                          __uint_as_float(o[4 * q + 3]) * inv_l);
+        __syncwarp();
+#pragma unroll
+        for (int rr = 0; rr < 32; rr += 4) {
+          const int hh = rr + (lane >> 3), q = lane & 7;
+          *reinterpret_cast<float4*>(obase + (int64_t)hh * kDv + c0 + 4 * q) =
+              stage[hh * 8 + (q ^ (hh & 7))];
+        }
+        __syncwarp();
       }
-    } else if (ok) {
-      for (int c0 = 0; c0 < 256; c0 += 4)
-        *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (ok && r == 0 && p.lse != nullptr)
       p.lse[(int64_t)n * kHeads + h] =
