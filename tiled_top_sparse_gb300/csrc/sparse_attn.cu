@@ -264,11 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_16(dst + i * kSlabBytes, src_row + g * 64, src_bytes);
         }
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(kside ? &bar_kfull[st] : &bar_vfull[st]));
+      // Arrive when this thread's copies have landed, without waiting for them here: the
+      // next tile's copies go out while these are in flight (the MMA warp orders the
+      // landed data for the tensor core with a proxy fence after its wait).
+      cp_async_arrive_noinc(smem_u32(kside ? &bar_kfull[st] : &bar_vfull[st]));
     }
+    cp_async_wait_all();  // nothing may still be landing when the CTA exits
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the issue loop converged; the elected lane issues.
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = t & 1;
         if (!warp_wait(smem_u32(&bar_kfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
           return false;
+        fence_proxy_async_smem();  // gathered rows (generic proxy) -> tensor core reads
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kKOnly; ++i)
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = t & 1;
         if (!warp_wait(smem_u32(&bar_vfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
           return false;
+        fence_proxy_async_smem();
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kVSlabs; ++i)
