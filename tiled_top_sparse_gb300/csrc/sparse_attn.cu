@@ -124,28 +124,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int v = tid; v < p.kv_len; v += kThreads) counts[v] = 0;
   __syncthreads();
   int my_valid = 0;
-  for (int j = tid; j < (by_count ? p.topk : p.sort_n); j += kThreads) {
-    int key = 0x7FFFFFFF;
-    if (j < p.topk) {
-      const int32_t i = idx_row[j];
-      if (i != -1) {
-        bool ok = i >= 0 && i < p.kv_len && (i / p.page_size) < p.num_logical_pages;
-        if (ok) {
-          const int32_t pg = p.page_table[i / p.page_size];
-          ok = pg >= 0 && pg < p.num_pages;
-        }
-        if (ok) {
+  const int n_scan = by_count ? p.topk : p.sort_n;
+  for (int j0 = 0; j0 < n_scan; j0 += 4 * kThreads) {
+    // Four entries per thread per round: all index loads, then all page-table loads,
+    // so the global-memory round trips overlap instead of running one after another.
+    int32_t iv[4], pgv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * kThreads + tid;
+      iv[u] = (j < p.topk) ? idx_row[j] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int32_t i = iv[u];
+      const bool in = i >= 0 && i < p.kv_len && (i / p.page_size) < p.num_logical_pages;
+      pgv[u] = in ? p.page_table[i / p.page_size] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * kThreads + tid;
+      if (j >= n_scan) continue;
+      const int32_t i = iv[u];
+      int key = 0x7FFFFFFF;
+      if (i != -1 && j < p.topk) {
+        if (pgv[u] >= 0 && pgv[u] < p.num_pages) {
           key = i;
           ++my_valid;
         } else if (p.dev_status != nullptr) {
           atomicOr(p.dev_status, kDevIndexRange);
         }
       }
-    }
-    if (by_count) {
-      if (key != 0x7FFFFFFF) atomicAdd(&counts[key], 1);  // integer: order-independent
-    } else {
-      sorted[j] = key;
+      if (by_count) {
+        if (key != 0x7FFFFFFF) atomicAdd(&counts[key], 1);  // integer: order-independent
+      } else {
+        sorted[j] = key;
+      }
     }
   }
   if (my_valid) atomicAdd(&s_cnt, my_valid);
@@ -168,8 +181,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int before = 0;
     for (int w = 0; w < warp; ++w) before += s_wsum[w];
     int pos = before + incl - tot;
-    for (int v = v0; v < v1; ++v)
-      for (int c = counts[v]; c > 0; --c) sorted[pos++] = v;
+    // The sorted list holds physical KV rows (page-table resolved) in logical order.
+    for (int v = v0; v < v1; ++v) {
+      const int c = counts[v];
+      if (c == 0) continue;
+      const int32_t row = p.page_table[v / p.page_size] * p.page_size + v % p.page_size;
+      for (int k = 0; k < c; ++k) sorted[pos++] = row;
+    }
   } else {
     for (int size = 2; size <= p.sort_n; size <<= 1) {
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -190,6 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int cnt = s_cnt;
   const int n_tiles = (cnt + kTileN - 1) / kTileN;
+  if (!by_count) {  // the bitonic path sorted logical positions: resolve them now
+    for (int pos = tid; pos < cnt; pos += kThreads) {
+      const int32_t v = sorted[pos];
+      sorted[pos] = p.page_table[v / p.page_size] * p.page_size + v % p.page_size;
+    }
+    __syncthreads();
+  }
   // Producer lanes 0..15 of producer warp w keep the physical row of entry
   // 16 * (w & 3) + lane of every tile.
   int32_t my_row[kMaxTiles];
@@ -198,12 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int j = 0; j < kMaxTiles; ++j) {
       const int pos = j * kTileN + e;
-      int32_t row = -1;
-      if (pos < cnt) {
-        const int32_t i = sorted[pos];
-        row = p.page_table[i / p.page_size] * p.page_size + i % p.page_size;
-      }
-      my_row[j] = row;
+      my_row[j] = pos < cnt ? sorted[pos] : -1;
     }
   }
   tc_fence_before();
