@@ -17,10 +17,12 @@
 //     columns are also this CTA's V columns, held as the A operand of TS MMAs;
 //     S double buffer [128,192) [192,256); O half [256,512);
 //   * shared memory: the other 5 Q slabs (80 KB), and two stages of the gathered
-//     tile split into its 5 K-only slabs (40 KB) and 4 V slabs (32 KB);
-//   * warps 0-1 gather the K-only slabs, warps 2-3 the V slabs (16-byte cp.async
-//     into the 128-byte-swizzled layout the MMA reads), warp 4 issues MMAs,
-//     warps 8-11 run the softmax (one head per thread) and the epilogue.
+//     tile split into its 5 K-only slabs (40 KB) and 4 V slabs (32 KB); Q_lo passes
+//     through the (still idle) V stages on its way into TMEM;
+//   * warps 0-3 gather the K-only slabs (16-byte cp.async into the 128-byte-swizzled
+//     layout the MMA reads), warps 4-7 the V slabs (TMA tile::gather4, four rows per
+//     copy, same layout), warp 8 issues MMAs, warps 12-15 run the softmax (one head
+//     per thread); all 16 warps write the output.
 // Both CTAs of a query compute the same S and the same softmax bits; each
 // accumulates O for its 256 V columns (the S work is done twice so that no
 // partial scores have to be exchanged between SMs).
@@ -61,18 +63,32 @@ struct SparseParams {
   float scale, scale_log2;
 };
 
+// One TMA copy of four whole rows (tile::gather4): 64 columns of each of rows r0..r3 of a
+// 2-D tensor map whose box is {64, 1}, landing as four consecutive 128-byte rows of the
+// map's swizzled layout at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int x, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+
 __device__ __forceinline__ int kslab_of(int r, int i) {  // i-th K-only slab (global id)
   return r == 0 ? 4 + i : (i < 4 ? i : 8);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap qmap, const SparseParams p) {
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap kvmap, const SparseParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_qhi, bar_qlo, bar_kfull[2], bar_vfull[2], bar_kempty[2],
+  __shared__ __align__(8) uint64_t bar_qhi, bar_qlo_smem, bar_qlo, bar_kfull[2], bar_vfull[2], bar_kempty[2],
       bar_vempty[2], bar_s[2], bar_p[2], bar_o, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_cnt;
   __shared__ int s_wsum[kThreads / 32];
+  __shared__ float s_inv_l[kHeads];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x >> 1, r = blockIdx.x & 1;
@@ -88,10 +104,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     s_cnt = 0;
     mbar_init(smem_u32(&bar_qhi), 1);
+    mbar_init(smem_u32(&bar_qlo_smem), 1);
     mbar_init(smem_u32(&bar_qlo), 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_kfull[i]), 128);
-      mbar_init(smem_u32(&bar_vfull[i]), 128);
+      mbar_init(smem_u32(&bar_vfull[i]), 4);  // one expect-tx arrival per V warp
       mbar_init(smem_u32(&bar_kempty[i]), 1);
       mbar_init(smem_u32(&bar_vempty[i]), 1);
       mbar_init(smem_u32(&bar_s[i]), 1);
@@ -106,12 +123,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   __syncthreads();
-  // Q slabs that stay in shared memory: one TMA per slab, issued before the sort.
+  // All of Q by TMA, issued before the sort: the 5 slabs that stay in shared memory,
+  // and the 4 Q_lo slabs into the V stages (idle until Q_lo has moved on into TMEM).
   if (tid == 0) {
     prefetch_tmap(&qmap);
+    prefetch_tmap(&kvmap);
     mbar_arrive_expect_tx(smem_u32(&bar_qhi), kQhiBytes);
     for (int i = 0; i < kKOnly; ++i)
       tma_load_3d(sQhi + i * kQSlabBytes, &qmap, smem_u32(&bar_qhi), 64 * kslab_of(r, i), 0, n);
+    mbar_arrive_expect_tx(smem_u32(&bar_qlo_smem), kVSlabs * kQSlabBytes);
+    for (int i = 0; i < kVSlabs; ++i)
+      tma_load_3d(sV0 + i * kQSlabBytes, &qmap, smem_u32(&bar_qlo_smem), 64 * (4 * r + i), 0, n);
   }
 
   // ---- canonical order: validate, then sort the index list ascending ----
@@ -216,7 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
   // Producer lanes 0..15 of producer warp w keep the physical row of entry
-  // 16 * (w & 3) + lane of every tile.
+  // 16 * (w & 3) + lane of every tile. Entries past the list (last tile only) are
+  // copied from the last listed row, so every copy-engine coordinate is in range;
+  // the softmax gives them zero weight.
+  const int32_t fill_row = cnt > 0 ? sorted[cnt - 1] : 0;
   int32_t my_row[kMaxTiles];
   if (warp < 8) {
     const int e = 16 * (warp & 3) + (lane & 15);
@@ -234,36 +259,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------------------ Q_lo -> TMEM, gather
+    bool go = true;
     if (warp < 4) {
+      // Q_lo: from the V stages (landed by TMA, 128-byte-swizzled rows) into TMEM.
       const int h = tid;  // warp w covers TMEM lanes 32w..32w+31
-      const uint32_t* qrow =
-          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)n * kHeads + h) * kDqk);
-      for (int i = 0; i < kVSlabs; ++i) {
-        uint32_t v[32];
-        const uint4* src = reinterpret_cast<const uint4*>(qrow + (4 * r + i) * 32);
+      const bool okq = __all_sync(
+          0xFFFFFFFFu, mbar_wait(smem_u32(&bar_qlo_smem), 0, abort_flag, p.dev_status));
+      if (okq) {
+        const uint8_t* qrow = smem + kQhiBytes + 2 * kKStage + h * 128;
+#pragma unroll 1
+        for (int i = 0; i < kVSlabs; ++i) {
+          uint32_t v[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 x = __ldg(src + c);
-          v[4 * c] = x.x;
-          v[4 * c + 1] = x.y;
-          v[4 * c + 2] = x.z;
-          v[4 * c + 3] = x.w;
+          for (int c = 0; c < 8; ++c) {
+            const uint4 x =
+                *reinterpret_cast<const uint4*>(qrow + i * kQSlabBytes + ((c ^ (h & 7)) << 4));
+            v[4 * c] = x.x;
+            v[4 * c + 1] = x.y;
+            v[4 * c + 2] = x.z;
+            v[4 * c + 3] = x.w;
+          }
+          tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + i * 32, v);
         }
-        tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + i * 32, v);
+        tmem_st_wait();
       }
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_qlo));
+      mbar_arrive(smem_u32(&bar_qlo));  // also: the V stages are free for gathering
+    } else {
+      go = mbar_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status);
     }
     const bool kside = warp < 4;
     const int nslab = kside ? kKOnly : kVSlabs;
-    // Producer warp w of a role copies entries 16*(w&3) .. +15 of the tile. Lane l copies
-    // the 16-byte chunk (l & 7) of entry 16*(w&3) + 4*rr + (l >> 3), rr = 0..3, so one
-    // warp instruction moves four whole 128-byte row segments. Row offsets come from
-    // the lane that owns the entry (my_row), by shuffle.
+    // Producer warp w of a role copies entries 16*(w&3) .. +15 of the tile. K side: lane
+    // l copies the 16-byte chunk (l & 7) of entry 16*(w&3) + 4*rr + (l >> 3), rr = 0..3,
+    // so one warp instruction moves four whole 128-byte row segments. V side: lanes 0..3
+    // each issue one four-row TMA gather per slab. Row offsets come from the lane that
+    // owns the entry (my_row), by shuffle.
     const int e_base = 16 * (warp & 3);
     const int chunk = lane & 7;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; go && j < n_tiles; ++j) {
       const int st = j & 1;
       if (j >= 2) {
         const uint32_t eb = smem_u32(kside ? &bar_kempty[st] : &bar_vempty[st]);
@@ -271,6 +305,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int32_t own_row = my_row[j];
       const uint32_t stage = kside ? sK0 + st * kKStage : sV0 + st * kVStage;
+      if (!kside) {
+        const uint32_t fb = smem_u32(&bar_vfull[st]);
+        const int32_t own = own_row < 0 ? fill_row : own_row;
+        const int gi = lane & 3;
+        const int32_t r0 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi);
+        const int32_t r1 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi + 1);
+        const int32_t r2 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi + 2);
+        const int32_t r3 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi + 3);
+        if (lane == 0) mbar_arrive_expect_tx(fb, 16 * kVSlabs * 128);
+        __syncwarp();
+        if (lane < 4) {
+          const uint32_t dst = stage + (e_base + 4 * gi) * 128;
+#pragma unroll
+          for (int i = 0; i < kVSlabs; ++i)
+            tma_gather4(dst + i * kSlabBytes, &kvmap, fb, 64 * (4 * r + i), r0, r1, r2, r3);
+        }
+        continue;
+      }
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const int el = rr * 4 + (lane >> 3);  // entry within this warp's 16
@@ -287,9 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Arrive when this thread's copies have landed, without waiting for them here: the
       // next tile's copies go out while these are in flight (the MMA warp orders the
       // landed data for the tensor core with a proxy fence after its wait).
-      cp_async_arrive_noinc(smem_u32(kside ? &bar_kfull[st] : &bar_vfull[st]));
+      cp_async_arrive_noinc(smem_u32(&bar_kfull[st]));
     }
     cp_async_wait_all();  // nothing may still be landing when the CTA exits
+    if (!kside && lane == 0)  // nor any copy-engine gather
+      for (int j = (n_tiles > 2 ? n_tiles - 2 : 0); j < n_tiles; ++j)
+        mbar_wait(smem_u32(&bar_vfull[j & 1]), (j >> 1) & 1, nullptr, p.dev_status);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the issue loop converged; the elected lane issues.
@@ -329,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = t & 1;
         if (!warp_wait(smem_u32(&bar_vfull[st]), (t >> 1) & 1, abort_flag, p.dev_status))
           return false;
-        fence_proxy_async_smem();
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kVSlabs; ++i)
@@ -418,51 +472,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_p[st]));
     }
-    // ---- epilogue ----
     if (ok && n_tiles > 0)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_o), 0, abort_flag, p.dev_status));
-    tc_fence_after();
-    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    if (ok) {
-      // Each thread holds one head's 256 values; a 4 KB slice of the (now idle) gather
-      // stage per warp turns them into 128-byte segments, four heads per store.
-      float4* stage = reinterpret_cast<float4*>(smem + kQhiBytes + (warp & 3) * 4096);
-      const uint32_t O_row = tmem + 256 + lane_off;
-      float* obase = p.out + ((int64_t)n * kHeads + (warp & 3) * 32) * kDv + 256 * r;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 256; c0 += 32) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(O_row + c0, o);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          stage[lane * 8 + (q ^ (lane & 7))] =
-              make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                          __uint_as_float(o[4 * q + 2]) * inv_l,
-                          __uint_as_float(o[4 * q + 3]) * inv_l);
-        __syncwarp();
-#pragma unroll
-        for (int rr = 0; rr < 32; rr += 4) {
-          const int hh = rr + (lane >> 3), q = lane & 7;
-          *reinterpret_cast<float4*>(obase + (int64_t)hh * kDv + c0 + 4 * q) =
-              stage[hh * 8 + (q ^ (hh & 7))];
-        }
-        __syncwarp();
-      }
-    }
+    s_inv_l[h] = (l > 0.f) ? 1.f / l : 0.f;
     if (ok && r == 0 && p.lse != nullptr)
       p.lse[(int64_t)n * kHeads + h] =
           (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
   }
 
-  // The Q_hi copy must have landed before the CTA may exit (it is otherwise only
-  // waited for by the MMA thread, which skips its work when no entry is valid).
-  if (tid == 0) mbar_wait(smem_u32(&bar_qhi), 0, nullptr, p.dev_status);
+  // The Q copies must have landed before the CTA may exit (they are otherwise only
+  // waited for by roles that may have given up early).
+  if (tid == 0) {
+    mbar_wait(smem_u32(&bar_qhi), 0, nullptr, p.dev_status);
+    mbar_wait(smem_u32(&bar_qlo_smem), 0, nullptr, p.dev_status);
+  }
+  tc_fence_before();
+  __syncthreads();  // O is complete (bar_o) and every gather has landed
+  tc_fence_after();
+
+  // ---- epilogue: out = O / l, by all 16 warps ----
+  // Warp w reads TMEM lanes 32(w&3)..+31 (its heads) and columns 64(w>>2)..+63 of the
+  // O half; a 4 KB slice of the idle gather stages per warp turns each head's values
+  // into 128-byte segments, four heads per store.
+  if (*abort_flag == 0) {
+    const int hq = warp & 3;
+    float4* stage = reinterpret_cast<float4*>(smem + kQhiBytes + warp * 4096);
+    const uint32_t O_row = tmem + 256 + (static_cast<uint32_t>(hq * 32) << 16);
+    const float inv_l = s_inv_l[hq * 32 + lane];
+    float* obase = p.out + ((int64_t)n * kHeads + hq * 32) * kDv + 256 * r;
+#pragma unroll 1
+    for (int c0 = (warp >> 2) * 64; c0 < (warp >> 2) * 64 + 64; c0 += 32) {
+      uint32_t o[32];
+      if (n_tiles > 0) {
+        tmem_ld32(O_row + c0, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        stage[lane * 8 + (q ^ (lane & 7))] =
+            make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                        __uint_as_float(o[4 * q + 2]) * inv_l,
+                        __uint_as_float(o[4 * q + 3]) * inv_l);
+      __syncwarp();
+#pragma unroll
+      for (int rr = 0; rr < 32; rr += 4) {
+        const int hh = rr + (lane >> 3), q = lane & 7;
+        *reinterpret_cast<float4*>(obase + (int64_t)hh * kDv + c0 + 4 * q) =
+            stage[hh * 8 + (q ^ (hh & 7))];
+      }
+      __syncwarp();
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
@@ -483,6 +546,18 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
   CUresult rr = encode_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                                   const_cast<void*>(a.q), dims, strides, box,
                                   CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rr != CUDA_SUCCESS) {
+    *drv_err = (int)rr;
+    return cudaErrorInvalidValue;
+  }
+  // The cache as rows of 576 values for the four-row gathers (box: 64 columns x 1 row).
+  CUtensorMap kvmap;
+  const uint64_t kv_dims[2] = {(uint64_t)kDqk, (uint64_t)a.num_pages * a.page_size};
+  const uint64_t kv_strides[1] = {(uint64_t)kDqk * 2};
+  const uint32_t kv_box[2] = {64, 1};
+  rr = encode_tensor_map(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         const_cast<void*>(a.kv_cache), kv_dims, kv_strides, kv_box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (rr != CUDA_SUCCESS) {
     *drv_err = (int)rr;
     return cudaErrorInvalidValue;
@@ -509,7 +584,7 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<2 * a.nq, kThreads, kSmemBytes, stream>>>(qmap, p);
+  sparse_attn_kernel<<<2 * a.nq, kThreads, kSmemBytes, stream>>>(qmap, kvmap, p);
   return cudaGetLastError();
 }
 
