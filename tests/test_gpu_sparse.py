@@ -53,6 +53,27 @@ def test_parity_small(tts, nq, kv_len, topk):
     assert_lse_close(lse.cpu().numpy(), rl, "sparse lse")
 
 
+@pytest.mark.parametrize("nq,kv_len,page_size,topk", [
+    (2, 20000, 64, 2048),   # kv_len above the counting-sort range: bitonic sort
+    (2, 16000, 1, 2048),    # counting sort, page table too large to copy into the scratch
+    (2, 20000, 1, 1500),    # bitonic sort, page table read from global memory
+    (3, 3000, 1, 2048),     # one-row pages, page table copied into the scratch
+])
+def test_parity_sort_and_page_table_paths(tts, nq, kv_len, page_size, topk):
+    inp = W.sparse_inputs(nq=nq, kv_len=kv_len, page_size=page_size, topk=topk,
+                          seed=kv_len + page_size + topk)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run(tts, inp, status=st)
+    tts.check_status(st)
+    ro, rl, bad = ref(inp)
+    assert bad == 0
+    assert_close_attn(out.cpu().numpy(), ro, f"sparse kv_len={kv_len} page={page_size}")
+    assert_lse_close(lse.cpu().numpy(), rl, "sparse lse")
+    perm = W.permute_rows(inp.idx, seed=kv_len)
+    out_p, lse_p = run(tts, inp, idx=perm)
+    assert torch.equal(out_p, out) and torch.equal(lse_p, lse)
+
+
 def test_empty_slots_duplicates_and_bad_entries(tts):
     inp = W.sparse_inputs(nq=4, kv_len=700, topk=130, seed=50)
     idx = inp.idx.clone()

@@ -50,6 +50,9 @@ constexpr int kSmemBytes = kQhiBytes + 2 * kKStage + 2 * kVStage + 1024;
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxTiles = kMaxTopk / kTileN;         // 32
 constexpr int kCountCap = 16384;  // kv_len up to this uses a counting sort
+constexpr int kScratchInts = 2 * kKStage / 4;  // sort scratch: the K stages (80 KB)
+static_assert(kMaxTopk <= 4 * kThreads, "one round of four index loads per thread");
+static_assert(kCountCap + kMaxTopk <= kScratchInts, "counts and the sorted list fit");
 
 struct SparseParams {
   const uint16_t* q;  // bf16 bits [nq, 128, 576]
@@ -137,50 +140,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- canonical order: validate, then sort the index list ascending ----
-  // Scratch (the gather stages are still unused): counts [kv_len] then the sorted list.
-  int32_t* counts = reinterpret_cast<int32_t*>(smem + kQhiBytes);
-  int32_t* sorted = counts + kCountCap;
+  // Scratch in the (still unused) K stages: counts [kv_len] (counting sort only), a copy
+  // of the page table when it fits, then the sorted list.
   const int32_t* idx_row = p.idx + (int64_t)n * p.topk;
   const bool by_count = p.kv_len <= kCountCap;
-  if (by_count)
-    for (int v = tid; v < p.kv_len; v += kThreads) counts[v] = 0;
-  __syncthreads();
-  int my_valid = 0;
   const int n_scan = by_count ? p.topk : p.sort_n;
-  for (int j0 = 0; j0 < n_scan; j0 += 4 * kThreads) {
-    // Four entries per thread per round: all index loads, then all page-table loads,
-    // so the global-memory round trips overlap instead of running one after another.
-    int32_t iv[4], pgv[4];
+  const int n_counts = by_count ? p.kv_len : 0;
+  const int nlp = p.num_logical_pages;
+  const bool pt_cached = n_counts + nlp + n_scan <= kScratchInts;
+  int32_t* counts = reinterpret_cast<int32_t*>(smem + kQhiBytes);
+  int32_t* pt = counts + n_counts;
+  int32_t* sorted = pt + (pt_cached ? nlp : 0);
+  // The index loads go out first; their round trip overlaps the zeroing and the
+  // page-table copy.
+  int32_t iv[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u * kThreads + tid;
-      iv[u] = (j < p.topk) ? idx_row[j] : -1;
-    }
+  for (int u = 0; u < 4; ++u) {
+    const int j = u * kThreads + tid;
+    iv[u] = (j < p.topk) ? idx_row[j] : -1;
+  }
+  for (int v = tid; v < n_counts; v += kThreads) counts[v] = 0;
+  if (pt_cached)
+    for (int g = tid; g < nlp; g += kThreads) pt[g] = p.page_table[g];
+  __syncthreads();
+  auto page_of = [&](int g) -> int32_t { return pt_cached ? pt[g] : p.page_table[g]; };
+  int my_valid = 0;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int32_t i = iv[u];
-      const bool in = i >= 0 && i < p.kv_len && (i / p.page_size) < p.num_logical_pages;
-      pgv[u] = in ? p.page_table[i / p.page_size] : -1;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u * kThreads + tid;
-      if (j >= n_scan) continue;
-      const int32_t i = iv[u];
-      int key = 0x7FFFFFFF;
-      if (i != -1 && j < p.topk) {
-        if (pgv[u] >= 0 && pgv[u] < p.num_pages) {
-          key = i;
-          ++my_valid;
-        } else if (p.dev_status != nullptr) {
-          atomicOr(p.dev_status, kDevIndexRange);
-        }
+  for (int u = 0; u < 4; ++u) {
+    const int j = u * kThreads + tid;
+    if (j >= n_scan) continue;
+    const int32_t i = iv[u];
+    int key = 0x7FFFFFFF;
+    if (i != -1 && j < p.topk) {
+      const bool in = i >= 0 && i < p.kv_len && (i / p.page_size) < nlp;
+      const int32_t pg = in ? page_of(i / p.page_size) : -1;
+      if (pg >= 0 && pg < p.num_pages) {
+        key = i;
+        ++my_valid;
+      } else if (p.dev_status != nullptr) {
+        atomicOr(p.dev_status, kDevIndexRange);
       }
-      if (by_count) {
-        if (key != 0x7FFFFFFF) atomicAdd(&counts[key], 1);  // integer: order-independent
-      } else {
-        sorted[j] = key;
-      }
+    }
+    if (by_count) {
+      if (key != 0x7FFFFFFF) atomicAdd(&counts[key], 1);  // integer: order-independent
+    } else {
+      sorted[j] = key;
     }
   }
   if (my_valid) atomicAdd(&s_cnt, my_valid);
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int v = v0; v < v1; ++v) {
       const int c = counts[v];
       if (c == 0) continue;
-      const int32_t row = p.page_table[v / p.page_size] * p.page_size + v % p.page_size;
+      const int32_t row = page_of(v / p.page_size) * p.page_size + v % p.page_size;
       for (int k = 0; k < c; ++k) sorted[pos++] = row;
     }
   } else {
@@ -233,22 +237,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!by_count) {  // the bitonic path sorted logical positions: resolve them now
     for (int pos = tid; pos < cnt; pos += kThreads) {
       const int32_t v = sorted[pos];
-      sorted[pos] = p.page_table[v / p.page_size] * p.page_size + v % p.page_size;
+      sorted[pos] = page_of(v / p.page_size) * p.page_size + v % p.page_size;
     }
     __syncthreads();
   }
-  // Producer lanes 0..15 of producer warp w keep the physical row of entry
-  // 16 * (w & 3) + lane of every tile. Entries past the list (last tile only) are
-  // copied from the last listed row, so every copy-engine coordinate is in range;
-  // the softmax gives them zero weight.
+  // Producer warp w keeps, in registers, the physical rows of entries 16 * (w & 3) ..
+  // +15 of every tile: lane l holds entry l & 15 of the even tiles (l < 16) or of the
+  // odd tiles (l >= 16), oldest first, and drops the front one once that tile is issued.
+  // Entries past the list (last tile only) take the last listed row, so every copy
+  // stays in range; the softmax gives them zero weight.
   const int32_t fill_row = cnt > 0 ? sorted[cnt - 1] : 0;
-  int32_t my_row[kMaxTiles];
+  int32_t rows_q[kMaxTiles / 2];
   if (warp < 8) {
     const int e = 16 * (warp & 3) + (lane & 15);
 #pragma unroll
-    for (int j = 0; j < kMaxTiles; ++j) {
-      const int pos = j * kTileN + e;
-      my_row[j] = pos < cnt ? sorted[pos] : -1;
+    for (int k = 0; k < kMaxTiles / 2; ++k) {
+      const int pos = (2 * k + (lane >> 4)) * kTileN + e;
+      rows_q[k] = pos < cnt ? sorted[pos] : fill_row;
     }
   }
   tc_fence_before();
@@ -289,12 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       go = mbar_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status);
     }
     const bool kside = warp < 4;
-    const int nslab = kside ? kKOnly : kVSlabs;
     // Producer warp w of a role copies entries 16*(w&3) .. +15 of the tile. K side: lane
     // l copies the 16-byte chunk (l & 7) of entry 16*(w&3) + 4*rr + (l >> 3), rr = 0..3,
     // so one warp instruction moves four whole 128-byte row segments. V side: lanes 0..3
     // each issue one four-row TMA gather per slab. Row offsets come from the lane that
-    // owns the entry (my_row), by shuffle.
+    // owns the entry (rows_q), by shuffle.
     const int e_base = 16 * (warp & 3);
     const int chunk = lane & 7;
     for (int j = 0; go && j < n_tiles; ++j) {
@@ -303,16 +307,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t eb = smem_u32(kside ? &bar_kempty[st] : &bar_vempty[st]);
         if (!mbar_wait(eb, ((j >> 1) - 1) & 1, abort_flag, p.dev_status)) break;
       }
-      const int32_t own_row = my_row[j];
+      const int32_t mine = rows_q[0];
+      const int src = (j & 1) * 16;  // the lanes that hold this tile's rows
+      if ((lane >> 4) == (j & 1)) {
+#pragma unroll
+        for (int k = 0; k + 1 < kMaxTiles / 2; ++k) rows_q[k] = rows_q[k + 1];
+      }
       const uint32_t stage = kside ? sK0 + st * kKStage : sV0 + st * kVStage;
       if (!kside) {
         const uint32_t fb = smem_u32(&bar_vfull[st]);
-        const int32_t own = own_row < 0 ? fill_row : own_row;
         const int gi = lane & 3;
-        const int32_t r0 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi);
-        const int32_t r1 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi + 1);
-        const int32_t r2 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi + 2);
-        const int32_t r3 = __shfl_sync(0xFFFFFFFFu, own, 4 * gi + 3);
+        const int32_t r0 = __shfl_sync(0xFFFFFFFFu, mine, src + 4 * gi);
+        const int32_t r1 = __shfl_sync(0xFFFFFFFFu, mine, src + 4 * gi + 1);
+        const int32_t r2 = __shfl_sync(0xFFFFFFFFu, mine, src + 4 * gi + 2);
+        const int32_t r3 = __shfl_sync(0xFFFFFFFFu, mine, src + 4 * gi + 3);
         if (lane == 0) mbar_arrive_expect_tx(fb, 16 * kVSlabs * 128);
         __syncwarp();
         if (lane < 4) {
@@ -326,15 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const int el = rr * 4 + (lane >> 3);  // entry within this warp's 16
-        const int32_t row = __shfl_sync(0xFFFFFFFFu, own_row, el);
+        const int32_t row = __shfl_sync(0xFFFFFFFFu, mine, src + el);
         const int e = e_base + el;
-        const uint16_t* src_row = p.kv + (int64_t)(row < 0 ? 0 : row) * kDqk + chunk * 8;
-        const uint32_t src_bytes = row < 0 ? 0u : 16u;
+        const uint16_t* src_row = p.kv + (int64_t)row * kDqk + chunk * 8;
         const uint32_t dst = stage + e * 128 + ((chunk ^ (e & 7)) << 4);
-        for (int i = 0; i < nslab; ++i) {
-          const int g = kside ? kslab_of(r, i) : 4 * r + i;
-          cp_async_16(dst + i * kSlabBytes, src_row + g * 64, src_bytes);
-        }
+#pragma unroll
+        for (int i = 0; i < kKOnly; ++i)
+          cp_async_16(dst + i * kSlabBytes, src_row + kslab_of(r, i) * 64, 16);
       }
       // Arrive when this thread's copies have landed, without waiting for them here: the
       // next tile's copies go out while these are in flight (the MMA warp orders the
