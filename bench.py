@@ -205,6 +205,9 @@ class Step:
                                           self.var.q.shape[1], self.var.k.shape[1],
                                           self.var.q.shape[2], torch.bfloat16))
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # sparse workspace: partial results of the split last wave
+        self.ws_sp = torch.empty(max(16, tts.sparse_workspace_bytes(self.sp.q.shape[0])),
+                                 dtype=torch.uint8, device=dev)
         self.flops = {"vision": self.vis.flops(), "varlen": self.var.flops(),
                       "sparse": self.sp.flops()}
         self.topk_bytes = self.tk.bytes()
@@ -234,7 +237,8 @@ class Step:
         elif name == "sparse":
             q, kv, pt, ix = self.d_sp
             t.sparse_attn_paged(q, kv, pt, ix, self.sp.kv_len, self.sp.scale, dv=self.sp.dv,
-                                out=self.o_sp, lse=self.l_sp, status=self.status)
+                                out=self.o_sp, lse=self.l_sp, workspace=self.ws_sp,
+                                status=self.status)
 
     PARTS = ("vision", "varlen", "topk", "sparse")
 

@@ -152,15 +152,32 @@ tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows
  * page_table device int32 [num_logical_pages]
  * idx        device int32 [nq, topk]
  * out        device fp32 [nq, num_heads, dv];  lse device fp32 [nq, num_heads] or NULL
+ * workspace  device scratch, optional (NULL / 0 bytes: not used). With at least
+ *            tts_sparse_workspace_bytes(nq) bytes, the (query, V half) units of the last,
+ *            partial wave of CTAs each run as 2 or 4 CTAs over consecutive tiles of the
+ *            sorted list, and the last of them to finish merges their unnormalised
+ *            results (the online-softmax merge, in part order). The result stays
+ *            deterministic and order-invariant; split units round differently from
+ *            unsplit ones. Owned by the caller; calls that may overlap on the GPU need
+ *            separate workspaces.
  * Built shape: num_heads = 128, dqk = 576, dv = 512, 1 <= topk <= 2048,
- * page_size >= 1 (TTS_ERR_UNSUPPORTED otherwise). q and kv_cache 16-byte aligned.
+ * page_size >= 1 (TTS_ERR_UNSUPPORTED otherwise). q, kv_cache, out and workspace
+ * 16-byte aligned.
  */
 tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, int32_t dqk,
                                  int32_t dv, const void* kv_cache, int32_t num_pages,
                                  int32_t page_size, const int32_t* page_table,
                                  int32_t num_logical_pages, int32_t kv_len, const int32_t* idx,
                                  int32_t topk, float scale, float* out, float* lse,
-                                 uint32_t* dev_status, void* stream);
+                                 void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                 void* stream);
+
+/*
+ * Workspace bytes that let tts_sparse_attn_paged split the last wave of nq queries on
+ * the current device (0: no split for this shape, or no device). At most about
+ * 132 KB per SM.
+ */
+size_t tts_sparse_workspace_bytes(int32_t nq);
 
 /*
  * Diagnostics (no counterpart in the pages): launches one thread that waits on a

@@ -96,7 +96,7 @@ def test_attn_host_validation(L):
 
 def _sparse(L, **kw):
     a = dict(q=P, nq=4, H=128, dqk=576, dv=512, kv=P, pages=41, ps=64, pt=P, nlp=41, kv_len=2590,
-             idx=P, topk=2048, scale=0.04, out=P, lse=NUL, st=NUL, stream=NUL)
+             idx=P, topk=2048, scale=0.04, out=P, lse=NUL, ws=NUL, wsb=0, st=NUL, stream=NUL)
     a.update(kw)
     return L.tts_sparse_attn_paged(*a.values())
 
@@ -111,7 +111,16 @@ def test_sparse_host_validation(L):
     assert _sparse(L, scale=-1.0) == tts.TTS_ERR_INVALID_ARG
     assert _sparse(L, H=64) == tts.TTS_ERR_UNSUPPORTED
     assert _sparse(L, topk=2049) == tts.TTS_ERR_UNSUPPORTED
+    assert _sparse(L, ws=ctypes.c_void_p(0x1008), wsb=1 << 20) == tts.TTS_ERR_INVALID_ARG
     assert _sparse(L, nq=0) == tts.TTS_OK
+
+
+def test_sparse_workspace_bytes_without_device(L):
+    # No GPU here: no split is planned; with nq <= 0 never.
+    import torch
+    assert L.tts_sparse_workspace_bytes(0) == 0
+    if not torch.cuda.is_available():
+        assert L.tts_sparse_workspace_bytes(323) == 0
 
 
 def test_product_has_no_cpu_fallback():

@@ -74,6 +74,33 @@ def test_parity_sort_and_page_table_paths(tts, nq, kv_len, page_size, topk):
     assert torch.equal(out_p, out) and torch.equal(lse_p, lse)
 
 
+@pytest.mark.parametrize("nq", [5, 30, 76, 160])
+def test_split_last_wave_matches_unsplit_and_oracle(tts, nq):
+    # nq = 5 / 30: every unit split (4 / 2 parts); 76: whole waves only (no split on a
+    # 152-SM part); 160: a partial wave of split units after whole ones.
+    inp = W.sparse_inputs(nq=nq, kv_len=2590, topk=2048, seed=70 + nq)
+    q, kv, pt, ix = to_dev(inp)
+    ws = torch.empty(max(16, tts.sparse_workspace_bytes(nq)), dtype=torch.uint8, device="cuda")
+    a_out, a_lse = tts.sparse_attn_paged(q, kv, pt, ix, inp.kv_len, inp.scale, workspace=ws)
+    b_out, b_lse = tts.sparse_attn_paged(q, kv, pt, ix, inp.kv_len, inp.scale, workspace=ws)
+    assert torch.equal(a_out, b_out) and torch.equal(a_lse, b_lse)  # run to run
+    perm = W.permute_rows(inp.idx, seed=nq).to("cuda")
+    p_out, p_lse = tts.sparse_attn_paged(q, kv, pt, perm, inp.kv_len, inp.scale, workspace=ws)
+    assert torch.equal(a_out, p_out) and torch.equal(a_lse, p_lse)  # order invariant
+    u_out, u_lse = tts.sparse_attn_paged(q, kv, pt, ix, inp.kv_len, inp.scale, split=False)
+    rows = sorted({0, nq // 2, nq - 1})
+    ro, rl, _ = ref(inp, rows=rows)
+    for o, l, what in ((a_out, a_lse, "split"), (u_out, u_lse, "unsplit")):
+        assert_close_attn(o[rows].cpu().numpy(), ro, f"sparse {what} nq={nq}")
+        assert_lse_close(l[rows].cpu().numpy(), rl, f"sparse {what} lse")
+    # The two schedules agree to rounding: each part rounds its P to bf16 relative to its
+    # own reference maximum (relative step 2^-9), so outputs may differ by a few 2^-9 of
+    # their scale; lse differs only by fp32 rounding of the merged sums.
+    scale = u_out.abs().max().item()
+    assert (a_out - u_out).abs().max().item() <= 2.0 ** -7 * scale
+    assert (a_lse - u_lse).abs().max().item() < 1e-4
+
+
 def test_empty_slots_duplicates_and_bad_entries(tts):
     inp = W.sparse_inputs(nq=4, kv_len=700, topk=130, seed=50)
     idx = inp.idx.clone()

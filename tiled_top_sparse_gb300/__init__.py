@@ -45,6 +45,7 @@ EXPORTED = (
     "tts_attn_fwd_varlen",
     "tts_topk_select",
     "tts_sparse_attn_paged",
+    "tts_sparse_workspace_bytes",
     "tts_attn_fwd_varlen_f32_noalloc",
     "tts_debug_wait_timeout",
 )
@@ -82,8 +83,10 @@ def lib() -> ctypes.CDLL:
     L.tts_topk_select.argtypes = [P, i64, i32, P, P, i32, P, P, P]
     L.tts_topk_select.restype = ctypes.c_int
     L.tts_sparse_attn_paged.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, i32, i32, P, i32,
-                                        f32, P, P, P, P]
+                                        f32, P, P, P, ctypes.c_size_t, P, P]
     L.tts_sparse_attn_paged.restype = ctypes.c_int
+    L.tts_sparse_workspace_bytes.argtypes = [i32]
+    L.tts_sparse_workspace_bytes.restype = ctypes.c_size_t
     L.tts_attn_fwd_varlen_f32_noalloc.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, i32,
                                                   i32, i32, i32, f32, P, P, P, P]
     L.tts_attn_fwd_varlen_f32_noalloc.restype = ctypes.c_int
@@ -200,12 +203,18 @@ def topk_select(logits, row_starts, row_lens, k, idx=None, status=None):
     return idx
 
 
+def sparse_workspace_bytes(nq) -> int:
+    return int(lib().tts_sparse_workspace_bytes(int(nq)))
+
+
 def sparse_attn_paged(q, kv_cache, page_table, idx, kv_len, scale, dv=512, out=None, lse=None,
-                      status=None, want_lse=True):
+                      workspace=None, status=None, want_lse=True, split=True):
     """Order-invariant sparse attention through a page table (tts_sparse_attn_paged).
 
     q bf16 [nq, H, dqk], kv_cache bf16 [pages, page_size, dqk], page_table int32 [n_pages],
-    idx int32 [nq, topk]. Returns (out fp32 [nq, H, dv], lse fp32 [nq, H]).
+    idx int32 [nq, topk]. Returns (out fp32 [nq, H, dv], lse fp32 [nq, H]). With split
+    (default) a workspace for the split of the last wave is passed (allocated here when
+    `workspace` is missing or too small); split=False passes none.
     """
     _cuda_contig(q, "q", torch.bfloat16)
     _cuda_contig(kv_cache, "kv_cache", torch.bfloat16)
@@ -220,9 +229,17 @@ def sparse_attn_paged(q, kv_cache, page_table, idx, kv_len, scale, dv=512, out=N
     _cuda_contig(out, "out", torch.float32)
     if lse is None and want_lse:
         lse = torch.empty((nq, H), dtype=torch.float32, device=q.device)
+    ws_bytes = 0
+    if split:
+        need = sparse_workspace_bytes(nq)
+        if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    else:
+        workspace = None
     code = lib().tts_sparse_attn_paged(
         _ptr(q), nq, H, dqk, int(dv), _ptr(kv_cache), pages, page_size, _ptr(page_table),
         page_table.numel(), int(kv_len), _ptr(idx), idx.shape[1], float(scale), _ptr(out),
-        _ptr(lse), _ptr(status), _stream(q.device))
+        _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(q.device))
     _check(code, "tts_sparse_attn_paged")
     return out, lse

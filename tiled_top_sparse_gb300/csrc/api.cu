@@ -179,15 +179,28 @@ tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows
                                       dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+size_t tts_sparse_workspace_bytes(int32_t nq) {
+  if (nq <= 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();  // no device: report no split
+    return 0;
+  }
+  return sparse_split_workspace_bytes(nq, sms);
+}
+
 tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, int32_t dqk,
                                  int32_t dv, const void* kv_cache, int32_t num_pages,
                                  int32_t page_size, const int32_t* page_table,
                                  int32_t num_logical_pages, int32_t kv_len, const int32_t* idx,
                                  int32_t topk, float scale, float* out, float* lse,
-                                 uint32_t* dev_status, void* stream) {
+                                 void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                 void* stream) {
   if (q == nullptr || kv_cache == nullptr || page_table == nullptr || idx == nullptr ||
       out == nullptr)
     return TTS_ERR_INVALID_ARG;
+  if (workspace != nullptr && !aligned16(workspace)) return TTS_ERR_INVALID_ARG;
   if (nq < 0 || num_heads < 1 || dqk < 1 || dv < 1 || dv > dqk || num_pages < 1 ||
       page_size < 1 || num_logical_pages < 0 || kv_len < 0 || topk < 1)
     return TTS_ERR_INVALID_ARG;
@@ -213,6 +226,8 @@ tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, i
   a.scale = scale;
   a.out = out;
   a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace == nullptr ? 0 : workspace_bytes;
   a.dev_status = dev_status;
   int drv = 0;
   cudaError_t e = launch_sparse_attn(a, &drv, static_cast<cudaStream_t>(stream));

@@ -42,9 +42,14 @@ struct SparseArgs {
   float scale;
   float* out;
   float* lse;
+  void* workspace;  // optional: enables the split of the last, partial wave
+  size_t workspace_bytes;
   uint32_t* dev_status;
 };
 cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t stream);
+// Workspace bytes with which launch_sparse_attn splits the last wave of nq queries on a
+// device with `sms` SMs (0: no split for this shape).
+size_t sparse_split_workspace_bytes(int nq, int sms);
 
 // ---- tensor maps (driver entry point fetched through the runtime)
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,

@@ -51,6 +51,9 @@ constexpr int kMaxTopk = 2048;
 constexpr int kMaxTiles = kMaxTopk / kTileN;         // 32
 constexpr int kCountCap = 16384;  // kv_len up to this uses a counting sort
 constexpr int kScratchInts = 2 * kKStage / 4;  // sort scratch: the K stages (80 KB)
+constexpr int kMaxParts = 4;
+// One partial result: O [128 heads][256 columns], then m [128] and l [128].
+constexpr int kSlotFloats = kHeads * 256 + 2 * kHeads;
 static_assert(kMaxTopk <= 4 * kThreads, "one round of four index loads per thread");
 static_assert(kCountCap + kMaxTopk <= kScratchInts, "counts and the sorted list fit");
 
@@ -64,6 +67,12 @@ struct SparseParams {
   uint32_t* dev_status;
   int nq, num_pages, page_size, num_logical_pages, kv_len, topk, sort_n;
   float scale, scale_log2;
+  // Split of the last, partial wave: CTAs [0, n_main) are whole units (query, V half);
+  // each later unit runs as `parts` CTAs over consecutive tile ranges, whose partial
+  // results (unnormalised O, m, l) go to `partial` and are merged by the last finisher.
+  int n_main, parts;
+  float* partial;  // [tail units][parts][kSlotFloats]
+  uint32_t* done;  // [tail units], zero at launch
 };
 
 // One TMA copy of four whole rows (tile::gather4): 64 columns of each of rows r0..r3 of a
@@ -92,9 +101,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort, s_cnt;
   __shared__ int s_wsum[kThreads / 32];
   __shared__ float s_inv_l[kHeads];
+  __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x >> 1, r = blockIdx.x & 1;
+  int u = blockIdx.x, part = 0, nparts = 1;
+  if (u >= p.n_main) {
+    const int k = u - p.n_main;
+    u = p.n_main + k / p.parts;
+    part = k % p.parts;
+    nparts = p.parts;
+  }
+  const int n = u >> 1, r = u & 1;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -234,6 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int cnt = s_cnt;
   const int n_tiles = (cnt + kTileN - 1) / kTileN;
+  // This CTA's tiles of the sorted list (all of them unless the unit is split).
+  const int t_begin = part * n_tiles / nparts;
+  const int nt = (part + 1) * n_tiles / nparts - t_begin;
   if (!by_count) {  // the bitonic path sorted logical positions: resolve them now
     for (int pos = tid; pos < cnt; pos += kThreads) {
       const int32_t v = sorted[pos];
@@ -252,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = 16 * (warp & 3) + (lane & 15);
 #pragma unroll
     for (int k = 0; k < kMaxTiles / 2; ++k) {
-      const int pos = (2 * k + (lane >> 4)) * kTileN + e;
+      const int pos = (t_begin + 2 * k + (lane >> 4)) * kTileN + e;
       rows_q[k] = pos < cnt ? sorted[pos] : fill_row;
     }
   }
@@ -301,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // owns the entry (rows_q), by shuffle.
     const int e_base = 16 * (warp & 3);
     const int chunk = lane & 7;
-    for (int j = 0; go && j < n_tiles; ++j) {
+    for (int j = 0; go && j < nt; ++j) {
       const int st = j & 1;
       if (j >= 2) {
         const uint32_t eb = smem_u32(kside ? &bar_kempty[st] : &bar_vempty[st]);
@@ -349,12 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cp_async_wait_all();  // nothing may still be landing when the CTA exits
     if (!kside && lane == 0)  // nor any copy-engine gather
-      for (int j = (n_tiles > 2 ? n_tiles - 2 : 0); j < n_tiles; ++j)
+      for (int j = (nt > 2 ? nt - 2 : 0); j < nt; ++j)
         mbar_wait(smem_u32(&bar_vfull[j & 1]), (j >> 1) & 1, nullptr, p.dev_status);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the issue loop converged; the elected lane issues.
-    if (n_tiles > 0) {
+    if (nt > 0) {
       const uint32_t e = elect_one();
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTileN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, 0, 1);
@@ -404,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // while S_v(t), S_k(t+1) and PV(t) ran; softmax(t+1) overlaps S_k(t+2).
       if (ok) {
         tc_fence_after();
-        ok = issue_s_k(0) && issue_s_v(0) && (n_tiles < 2 || issue_s_k(1));
+        ok = issue_s_k(0) && issue_s_v(0) && (nt < 2 || issue_s_k(1));
       }
-      for (int j = 0; ok && j < n_tiles; ++j) {
+      for (int j = 0; ok && j < nt; ++j) {
         const int st = j & 1;
         if (!warp_wait(smem_u32(&bar_p[st]), (j >> 1) & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
@@ -415,9 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts_elect(O_t, S_t[st] + ks * 8, dvn[st] + ((ks * 2048) >> 4), idesc_pv,
                        (j > 0 || ks > 0) ? 1u : 0u, e);
         mma_commit_elect(smem_u32(&bar_vempty[st]), e);
-        if (j + 1 == n_tiles) mma_commit_elect(smem_u32(&bar_o), e);
-        if (j + 1 < n_tiles && !issue_s_v(j + 1)) break;
-        if (j + 2 < n_tiles && !issue_s_k(j + 2)) break;
+        if (j + 1 == nt) mma_commit_elect(smem_u32(&bar_o), e);
+        if (j + 1 < nt && !issue_s_v(j + 1)) break;
+        if (j + 2 < nt && !issue_s_k(j + 2)) break;
       }
       mma_commit_elect(smem_u32(&bar_drain), e);
       mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
@@ -429,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; j < nt; ++j) {
       const int st = j & 1;
       const uint32_t S_row = tmem + 128 + st * 64 + lane_off;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_s[st]), (j >> 1) & 1, abort_flag,
@@ -441,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float pm1 = tmem_ld32_max(S_row + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
       float* s = reinterpret_cast<float*>(sr);
-      const int valid = cnt - j * kTileN;  // entries of this tile that exist
+      const int valid = cnt - (t_begin + j) * kTileN;  // entries of this tile that exist
       float tile_max = fmaxf(pm0, pm1);
       if (valid < kTileN) {  // entries past the list must not count in the max
 #pragma unroll
@@ -478,12 +498,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_p[st]));
     }
-    if (ok && n_tiles > 0)
+    if (ok && nt > 0)
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_o), 0, abort_flag, p.dev_status));
-    s_inv_l[h] = (l > 0.f) ? 1.f / l : 0.f;
-    if (ok && r == 0 && p.lse != nullptr)
-      p.lse[(int64_t)n * kHeads + h] =
-          (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
+    if (nparts == 1) {
+      s_inv_l[h] = (l > 0.f) ? 1.f / l : 0.f;
+      if (ok && r == 0 && p.lse != nullptr)
+        p.lse[(int64_t)n * kHeads + h] =
+            (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
+    } else {  // a part: O stays unnormalised; m and l go next to it
+      s_inv_l[h] = 1.f;
+      float* ml = p.partial + (int64_t)((u - p.n_main) * nparts + part) * kSlotFloats +
+                  kHeads * 256;
+      ml[h] = m_ref;
+      ml[kHeads + h] = l;
+    }
   }
 
   // The Q copies must have landed before the CTA may exit (they are otherwise only
@@ -496,20 +524,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();  // O is complete (bar_o) and every gather has landed
   tc_fence_after();
 
-  // ---- epilogue: out = O / l, by all 16 warps ----
+  // ---- epilogue: out = O / l (or a part's O, to its slot), by all 16 warps ----
   // Warp w reads TMEM lanes 32(w&3)..+31 (its heads) and columns 64(w>>2)..+63 of the
   // O half; a 4 KB slice of the idle gather stages per warp turns each head's values
   // into 128-byte segments, four heads per store.
-  if (*abort_flag == 0) {
+  const bool fine = *abort_flag == 0;  // stable: every role has finished
+  if (fine) {
     const int hq = warp & 3;
     float4* stage = reinterpret_cast<float4*>(smem + kQhiBytes + warp * 4096);
     const uint32_t O_row = tmem + 256 + (static_cast<uint32_t>(hq * 32) << 16);
     const float inv_l = s_inv_l[hq * 32 + lane];
-    float* obase = p.out + ((int64_t)n * kHeads + hq * 32) * kDv + 256 * r;
+    const int64_t ostride = nparts == 1 ? kDv : 256;
+    float* obase =
+        nparts == 1
+            ? p.out + ((int64_t)n * kHeads + hq * 32) * kDv + 256 * r
+            : p.partial + (int64_t)((u - p.n_main) * nparts + part) * kSlotFloats + hq * 32 * 256;
 #pragma unroll 1
     for (int c0 = (warp >> 2) * 64; c0 < (warp >> 2) * 64 + 64; c0 += 32) {
       uint32_t o[32];
-      if (n_tiles > 0) {
+      if (nt > 0) {
         tmem_ld32(O_row + c0, o);
         tmem_ld_wait();
       } else {
@@ -526,10 +559,67 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int rr = 0; rr < 32; rr += 4) {
         const int hh = rr + (lane >> 3), q = lane & 7;
-        *reinterpret_cast<float4*>(obase + (int64_t)hh * kDv + c0 + 4 * q) =
+        *reinterpret_cast<float4*>(obase + (int64_t)hh * ostride + c0 + 4 * q) =
             stage[hh * 8 + (q ^ (hh & 7))];
       }
       __syncwarp();
+    }
+  }
+  if (nparts > 1 && fine) {
+    // The last part of the unit to finish merges all parts in part order:
+    //   out = sum_p w_p O_p / sum_p w_p l_p,  w_p = 2^((m_p - M) * scale * log2 e),
+    //   M = max_p m_p  (the online-softmax merge, with a fixed order).
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&p.done[u - p.n_main], 1u) == (uint32_t)(nparts - 1);
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const float* slot0 = p.partial + (int64_t)(u - p.n_main) * nparts * kSlotFloats;
+      // merge weights [part][head], in the idle gather stages (the staging is done)
+      float* s_w = reinterpret_cast<float*>(smem + kQhiBytes);
+      if (tid < kHeads) {
+        float mp[kMaxParts], w[kMaxParts];
+        float M = -INFINITY;
+#pragma unroll
+        for (int pp = 0; pp < kMaxParts; ++pp)
+          if (pp < nparts) {
+            mp[pp] = __ldcg(slot0 + pp * kSlotFloats + kHeads * 256 + tid);
+            M = fmaxf(M, mp[pp]);
+          }
+        float L = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < kMaxParts; ++pp)
+          if (pp < nparts) {
+            w[pp] = (mp[pp] == -INFINITY) ? 0.f : ex2_approx((mp[pp] - M) * p.scale_log2);
+            L += __ldcg(slot0 + pp * kSlotFloats + kHeads * 256 + kHeads + tid) * w[pp];
+          }
+        const float inv_L = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+        for (int pp = 0; pp < kMaxParts; ++pp)
+          if (pp < nparts) s_w[pp * kHeads + tid] = w[pp] * inv_L;
+        if (r == 0 && p.lse != nullptr)
+          p.lse[(int64_t)n * kHeads + tid] =
+              (L > 0.f) ? M * p.scale + log2f(L) * 0.69314718055994531f : -INFINITY;
+      }
+      __syncthreads();
+      float* obase = p.out + (int64_t)n * kHeads * kDv + 256 * r;
+      for (int i = tid; i < kHeads * 64; i += kThreads) {
+        const int hh = i >> 6, c4 = i & 63;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int pp = 0; pp < kMaxParts; ++pp)
+          if (pp < nparts) {
+            const float4 v =
+                __ldcg(reinterpret_cast<const float4*>(slot0 + pp * kSlotFloats + hh * 256) + c4);
+            const float wq = s_w[pp * kHeads + hh];
+            acc.x = fmaf(v.x, wq, acc.x);
+            acc.y = fmaf(v.y, wq, acc.y);
+            acc.z = fmaf(v.z, wq, acc.z);
+            acc.w = fmaf(v.w, wq, acc.w);
+          }
+        *reinterpret_cast<float4*>(obase + (int64_t)hh * kDv + 4 * c4) = acc;
+      }
     }
   }
   tc_fence_before();
@@ -540,7 +630,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The split of the last wave: with U = 2 nq units on `sms` SMs, the U mod sms units of
+// the partial wave run as `parts` CTAs each (4 if they still fit in one wave, else 2).
+struct SplitPlan {
+  int tail = 0, parts = 1;
+  size_t done_bytes = 0, bytes = 0;
+};
+SplitPlan plan_split(int nq, int sms) {
+  SplitPlan s;
+  const int units = 2 * nq;
+  const int tail = sms > 0 ? units % sms : 0;
+  if (tail == 0) return s;
+  for (int parts = kMaxParts; parts >= 2; parts /= 2)
+    if (tail * parts <= sms) {
+      s.tail = tail;
+      s.parts = parts;
+      s.done_bytes = ((size_t)tail * 4 + 255) / 256 * 256;
+      s.bytes = s.done_bytes + (size_t)tail * parts * kSlotFloats * sizeof(float);
+      break;
+    }
+  return s;
+}
+
 }  // namespace
+
+size_t sparse_split_workspace_bytes(int nq, int sms) { return plan_split(nq, sms).bytes; }
 
 cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t stream) {
   if (a.heads != kHeads || a.dqk != kDqk || a.dv != kDv || a.topk > kMaxTopk)
@@ -587,10 +701,32 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
   p.sort_n = sort_n;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  const int units = 2 * a.nq;
+  p.n_main = units;
+  p.parts = 1;
+  p.partial = nullptr;
+  p.done = nullptr;
+  int grid = units;
+  if (a.workspace != nullptr) {
+    int dev = 0, sms = 0;
+    cudaError_t ea = cudaGetDevice(&dev);
+    if (ea == cudaSuccess) ea = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (ea != cudaSuccess) return ea;
+    const SplitPlan sp = plan_split(a.nq, sms);
+    if (sp.parts > 1 && a.workspace_bytes >= sp.bytes) {
+      p.done = static_cast<uint32_t*>(a.workspace);
+      p.partial = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + sp.done_bytes);
+      p.n_main = units - sp.tail;
+      p.parts = sp.parts;
+      grid = p.n_main + sp.tail * sp.parts;
+      ea = cudaMemsetAsync(p.done, 0, (size_t)sp.tail * 4, stream);
+      if (ea != cudaSuccess) return ea;
+    }
+  }
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<2 * a.nq, kThreads, kSmemBytes, stream>>>(qmap, kvmap, p);
+  sparse_attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kvmap, p);
   return cudaGetLastError();
 }
 
