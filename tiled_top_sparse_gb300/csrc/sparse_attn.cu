@@ -66,6 +66,7 @@ struct SparseParams {
   float* lse;
   uint32_t* dev_status;
   int nq, num_pages, page_size, num_logical_pages, kv_len, topk, sort_n;
+  int page_shift;  // log2(page_size) when it is a power of two, else -1
   float scale, scale_log2;
   // Split of the last, partial wave: CTAs [0, n_main) are whole units (query, V half);
   // each later unit runs as `parts` CTAs over consecutive tile ranges, whose partial
@@ -181,6 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int g = tid; g < nlp; g += kThreads) pt[g] = p.page_table[g];
   __syncthreads();
   auto page_of = [&](int g) -> int32_t { return pt_cached ? pt[g] : p.page_table[g]; };
+  // logical position -> (logical page, offset); shifts for power-of-two page sizes
+  auto lpage = [&](int v) { return p.page_shift >= 0 ? v >> p.page_shift : v / p.page_size; };
+  auto row_of = [&](int v) -> int32_t {
+    const int g = lpage(v);
+    return page_of(g) * p.page_size + (v - g * p.page_size);
+  };
   int my_valid = 0;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -189,8 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t i = iv[u];
     int key = 0x7FFFFFFF;
     if (i != -1 && j < p.topk) {
-      const bool in = i >= 0 && i < p.kv_len && (i / p.page_size) < nlp;
-      const int32_t pg = in ? page_of(i / p.page_size) : -1;
+      const bool in = i >= 0 && i < p.kv_len && lpage(i) < nlp;
+      const int32_t pg = in ? page_of(lpage(i)) : -1;
       if (pg >= 0 && pg < p.num_pages) {
         key = i;
         ++my_valid;
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int v = v0; v < v1; ++v) {
       const int c = counts[v];
       if (c == 0) continue;
-      const int32_t row = page_of(v / p.page_size) * p.page_size + v % p.page_size;
+      const int32_t row = row_of(v);
       for (int k = 0; k < c; ++k) sorted[pos++] = row;
     }
   } else {
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!by_count) {  // the bitonic path sorted logical positions: resolve them now
     for (int pos = tid; pos < cnt; pos += kThreads) {
       const int32_t v = sorted[pos];
-      sorted[pos] = page_of(v / p.page_size) * p.page_size + v % p.page_size;
+      sorted[pos] = row_of(v);
     }
     __syncthreads();
   }
@@ -693,6 +700,9 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
   p.nq = a.nq;
   p.num_pages = a.num_pages;
   p.page_size = a.page_size;
+  p.page_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == a.page_size) p.page_shift = sh;
   p.num_logical_pages = a.num_logical_pages;
   p.kv_len = a.kv_len;
   p.topk = a.topk;
