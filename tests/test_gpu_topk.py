@@ -59,6 +59,28 @@ def test_heavy_ties_and_signed_zero(tts):
     assert np.array_equal(run(tts, inp).cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("pattern", ["constant", "signed_zeros", "low_byte", "full_fp32"])
+def test_digit_patterns(tts, pattern):
+    # The radix passes skip digits that are equal across a window; these rows make 4, 4,
+    # 3 and no passes skippable.
+    g = torch.Generator().manual_seed(31)
+    rows, cols = 12, 2590
+    if pattern == "constant":
+        x = torch.full((rows, cols), 0.375)
+    elif pattern == "signed_zeros":
+        x = torch.where(torch.rand(rows, cols, generator=g) < 0.5, torch.tensor(0.0),
+                        torch.tensor(-0.0))
+    elif pattern == "low_byte":  # 1.0 plus 0..255 units in the last place
+        bits = torch.randint(0, 256, (rows, cols), generator=g, dtype=torch.int32) + 0x3F800000
+        x = bits.view(torch.float32)
+    else:
+        x = torch.randn(rows, cols, generator=g)
+    inp = W.TopkInputs(x, torch.zeros(rows, dtype=torch.int32),
+                       torch.full((rows,), cols, dtype=torch.int32), 2048)
+    ref, _ = oracle_idx(inp)
+    assert np.array_equal(run(tts, inp).cpu().numpy(), ref)
+
+
 def test_short_rows_offsets_and_bad_windows(tts):
     g = torch.Generator().manual_seed(10)
     x = torch.randn(6, 3000, generator=g).to(torch.bfloat16).float()

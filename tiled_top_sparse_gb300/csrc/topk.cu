@@ -81,19 +81,62 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
   uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + 12 * kSortMax);  // [kWarps][256]
   __shared__ uint32_t digit_base[256];
   __shared__ int warp_tot[kWarps];
+  __shared__ uint32_t s_or[2], s_and[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = (n + kTopkThreads - 1) / kTopkThreads;  // steps per warp (<= 8)
   const int wbase = warp * 32 * E;
   const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t* wcnt = cnt + warp * 256;
+  // Passes that cannot change the order are skipped. Digit p < 3 of a key is a
+  // function of the sign alone when digit p of the raw float bits (-0 as +0) is the
+  // same across the window; the sign sits in digit 3, so keys that agree on the passes
+  // that run agree on such digits too, and the stable sort is unchanged without them.
+  // Digit 3 is skipped only if it is itself constant (then the pass is the identity).
+  if (tid < 2) {
+    s_or[tid] = 0u;
+    s_and[tid] = 0xFFFFFFFFu;
+  }
+  uint32_t key[kSortPerThread];
+  uint32_t k_or = 0u, k_and = 0xFFFFFFFFu, r_or = 0u, r_and = 0xFFFFFFFFu;
+#pragma unroll
+  for (int st = 0; st < kSortPerThread; ++st) {
+    const int idx = wbase + 32 * st + lane;
+    key[st] = 0u;
+    if (st < E && idx < n) {
+      uint32_t u = __float_as_uint(__ldg(src + idx));
+      if ((u & 0x7FFFFFFFu) == 0) u = 0;
+      key[st] = ~((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+      k_or |= key[st];
+      k_and &= key[st];
+      r_or |= u;
+      r_and &= u;
+    }
+  }
+  k_or = __reduce_or_sync(0xFFFFFFFFu, k_or);
+  k_and = __reduce_and_sync(0xFFFFFFFFu, k_and);
+  r_or = __reduce_or_sync(0xFFFFFFFFu, r_or);
+  r_and = __reduce_and_sync(0xFFFFFFFFu, r_and);
+  __syncthreads();
+  if (lane == 0) {
+    atomicOr(&s_or[0], k_or);
+    atomicAnd(&s_and[0], k_and);
+    atomicOr(&s_or[1], r_or);
+    atomicAnd(&s_and[1], r_and);
+  }
+  __syncthreads();
+  const uint32_t key_var = s_or[0] ^ s_and[0], raw_var = s_or[1] ^ s_and[1];
+  int in = 0;             // buffer holding the current order
+  bool from_regs = true;  // no pass has run yet: keys in registers, positions = indices
   for (int pass = 0; pass < 4; ++pass) {
-    const int in = pass & 1;
     const int shift = 8 * pass;
+    if (((key_var >> shift) & 0xFFu) == 0u ||
+        (pass < 3 && ((raw_var >> shift) & 0xFFu) == 0u))
+      continue;
     for (int d = lane; d < 256; d += 32) wcnt[d] = 0u;
     __syncwarp();
     // Per element: its key, and (position << 16 | rank within its digit and warp); the
     // digit is recomputed from the key. Both fit 16 bits (n <= 4096).
-    uint32_t key[kSortPerThread], pr[kSortPerThread];
+    uint32_t pr[kSortPerThread];
 #pragma unroll
     for (int st = 0; st < kSortPerThread; ++st) {
       if (st < E) {
@@ -101,8 +144,7 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
         const bool present = idx < n;
         uint32_t pos = 0;
         if (present) {
-          if (pass == 0) {
-            key[st] = ~ordered_key(__ldg(src + idx));
+          if (from_regs) {
             pos = static_cast<uint32_t>(idx);
           } else {
             key[st] = key_buf[in * kSortMax + idx];
@@ -146,9 +188,12 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
       }
     }
     __syncthreads();
+    in ^= 1;
+    from_regs = false;
   }
-  // Four passes: the sorted data is back in buffer 0.
-  for (int j = tid; j < k; j += kTopkThreads) out[j] = (j < n) ? (int32_t)pos_buf[j] : -1;
+  // No pass ran: every key is equal and the order is the positions'.
+  for (int j = tid; j < k; j += kTopkThreads)
+    out[j] = (j < n) ? (from_regs ? j : (int32_t)pos_buf[in * kSortMax + j]) : -1;
 }
 
 // Three CTAs per SM (<= 40 registers a thread): 456 resident rows on 152 SMs.
