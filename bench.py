@@ -293,6 +293,60 @@ class Step:
         return units
 
 
+def topk_protocol(step, dev, peaks):
+    """Top-k beyond the step: a ~6 MB launch is shorter than launch latency, so (1) a CUDA
+    graph of 256 launches rotating over 64 input/output buffer sets (384 MB, > 2x L2, so
+    every launch reads from HBM), graph time / launches; (2) one call over 16 x the rows
+    (the same rows repeated; its indices are checked against the single-batch result)."""
+    t = step.tts
+    lg, rs, rl = step.d_tk
+    k = step.tk.k
+    rows = lg.shape[0]
+    sets = [(lg.clone(), torch.empty((rows, k), dtype=torch.int32, device=dev))
+            for _ in range(64)]
+    n_launch = 256
+    s = torch.cuda.Stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for x, o in sets[:4]:
+            t.topk_select(x, rs, rl, k, idx=o, status=step.status)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n_launch):
+                x, o = sets[i % len(sets)]
+                t.topk_select(x, rs, rl, k, idx=o, status=step.status)
+        g.replay()
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n_launch
+    for _, o in sets:
+        assert torch.equal(o, sets[0][1]), "top-k: rotating buffer sets disagree"
+    reps = 16
+    big = (lg.repeat(reps, 1), rs.repeat(reps), rl.repeat(reps))
+    out_big = torch.empty((rows * reps, k), dtype=torch.int32, device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            t.topk_select(*big, k, idx=out_big, status=step.status)
+        e0.record(s)
+        for _ in range(10):
+            t.topk_select(*big, k, idx=out_big, status=step.status)
+        e1.record(s)
+    e1.synchronize()
+    us_big = e0.elapsed_time(e1) * 1e3 / 10
+    assert torch.equal(out_big, sets[0][1].repeat(reps, 1)), "top-k: scaled call disagrees"
+    gbs = step.topk_bytes / (us * 1e-6) / 1e9
+    gbs_big = reps * step.topk_bytes / (us_big * 1e-6) / 1e9
+    del sets, big, out_big
+    return {"graph_us_per_launch": us, "graph_rows_per_s": rows / (us * 1e-6),
+            "graph_gbs": gbs, "graph_frac_hbm": gbs / peaks["hbm_gbs"],
+            "graph_protocol": f"CUDA graph of {n_launch} launches over 64 rotating buffer sets",
+            "scaled_rows": rows * reps, "scaled_us": us_big,
+            "scaled_rows_per_s": rows * reps / (us_big * 1e-6), "scaled_gbs": gbs_big,
+            "scaled_frac_hbm": gbs_big / peaks["hbm_gbs"]}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(n_rows: int = 192, n_queries: int = 8):
     """Time the float64 oracle on bounded samples of each part.
@@ -480,6 +534,9 @@ def run_gpu(args, rank, world, local):
                       "gathered_bytes": step.gathered, "tflops": tf,
                       "frac_bf16_peak": tf / tensor_peak})
         comp[p] = c
+    if "topk" in parts and rank == 0:
+        comp["topk"].update(topk_protocol(step, dev, peaks))
+        tts.check_status(step.status, "bench top-k protocol")
     dom = max(parts, key=lambda p: comp[p]["ms"])
     dc = comp[dom]
     if dom in ("vision", "varlen"):
