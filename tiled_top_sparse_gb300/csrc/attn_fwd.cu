@@ -133,7 +133,8 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
 // sequences whose cu_seqlens entries are invalid.
 struct Item {
   int64_t q_start, k_start, Lq, Lk, q_lo;
-  int h, g, n_tiles;
+  int h, g, n_tiles;  // n_tiles: K/V tiles streamed = max(n0, n1)
+  int n0, n1;         // tiles each warpgroup needs (0: no rows, or no visible key)
 };
 __device__ __forceinline__ bool decode_item(const AttnParams& p, int it, Item& w, bool* bad) {
   const int h = it % p.hq;
@@ -151,13 +152,17 @@ __device__ __forceinline__ bool decode_item(const AttnParams& p, int it, Item& w
   }
   const int64_t q_lo = (int64_t)pr * 2 * kBlockM;  // first query row (within the sequence)
   if (q_lo >= Lq) return false;
-  int64_t kv_end = Lk;
-  if (p.causal) {
-    const int64_t i_last = (q_lo + 2 * kBlockM < Lq ? q_lo + 2 * kBlockM : Lq) - 1;
-    const int64_t lim = i_last + (Lk - Lq) + 1;
-    kv_end = lim < kv_end ? lim : kv_end;
-    if (kv_end < 0) kv_end = 0;
-  }
+  // Keys each warpgroup's rows can see: all of them, or (causal) up to its last row's
+  // diagonal; none for a warpgroup without rows (the odd last tile of a sequence).
+  auto keys_for = [&](int64_t r_first, int64_t r_end) -> int64_t {
+    if (r_first >= Lq) return 0;
+    if (!p.causal) return Lk;
+    const int64_t lim = (r_end < Lq ? r_end : Lq) - 1 + (Lk - Lq) + 1;
+    return lim < 0 ? 0 : (lim < Lk ? lim : Lk);
+  };
+  const int64_t kv_end0 = keys_for(q_lo, q_lo + kBlockM);
+  const int64_t kv_end1 = keys_for(q_lo + kBlockM, q_lo + 2 * kBlockM);
+  const int64_t kv_end = kv_end0 > kv_end1 ? kv_end0 : kv_end1;
   w.q_start = q_start;
   w.k_start = k_start;
   w.Lq = Lq;
@@ -166,6 +171,8 @@ __device__ __forceinline__ bool decode_item(const AttnParams& p, int it, Item& w
   w.h = h;
   w.g = h / (p.hq / p.hkv);
   w.n_tiles = (int)((kv_end + kBlockN - 1) / kBlockN);
+  w.n0 = (int)((kv_end0 + kBlockN - 1) / kBlockN);
+  w.n1 = (int)((kv_end1 + kBlockN - 1) / kBlockN);
   return true;
 }
 
@@ -357,7 +364,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       vd[i] = C::kTail ? smem_desc(sV(i), C::kVBoxBytes, 512, kSw64)
                        : smem_desc(sV(i), C::kBoxBytes, 1024, kSw128);
     }
-    int ni = 0, nq = 0, gt = 0;
+    // gt: K/V tiles so far (ring phases); g0 / g1: tiles of each warpgroup so far (S and P
+    // phases); nq: items with tiles (Q phases).
+    int ni = 0, nq = 0, gt = 0, g0 = 0, g1 = 0;
     bool ok = true;
     while (ok) {
       const int slot = ni & 1;
@@ -371,71 +380,130 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       Item w;
       bool bad;
       decode_item(p, it, w, &bad);
-      const int n = w.n_tiles;
+      const int n = w.n_tiles, n0 = w.n0, n1 = w.n1;
       if (n == 0) continue;
       const int st0 = gt % NS;
       ok = warp_wait(smem_u32(&bar_q[0]), nq & 1, abort_flag, p.dev_status) &&
            warp_wait(smem_u32(&bar_k[st0]), (gt / NS) & 1, abort_flag, p.dev_status);
       if (!ok) break;
       tc_fence_after();
-      issue_qk<D>(S_t[0], qd[0], kd[st0], qtd[0], ktd[st0], e);
-      mma_commit_elect(smem_u32(&bar_s[0]), e);
-      if (n == 1) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
+      if (n0 > 0) {
+        issue_qk<D>(S_t[0], qd[0], kd[st0], qtd[0], ktd[st0], e);
+        mma_commit_elect(smem_u32(&bar_s[0]), e);
+      }
+      if (n0 <= 1) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
       ok = warp_wait(smem_u32(&bar_q[1]), nq & 1, abort_flag, p.dev_status);
       if (!ok) break;
       tc_fence_after();
-      issue_qk<D>(S_t[1], qd[1], kd[st0], qtd[1], ktd[st0], e);
-      mma_commit_elect(smem_u32(&bar_s[1]), e);
+      if (n1 > 0) {
+        issue_qk<D>(S_t[1], qd[1], kd[st0], qtd[1], ktd[st0], e);
+        mma_commit_elect(smem_u32(&bar_s[1]), e);
+      }
       if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st0]), e);
-      if (n == 1) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
-      // Order on the tensor core: PV0(j) S0(j+1) PV1(j) S1(j+1).
-      for (int j = 0; j < n; ++j) {
+      if (n1 <= 1) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
+      // Order on the tensor core: PV0(j) S0(j+1) PV1(j) S1(j+1), each warpgroup only for
+      // the tiles its rows can see (its fully masked tiles are never computed). First the
+      // tiles after which both warpgroups still have one (the straight-line body), then
+      // the last one or two, where a warpgroup may stop or sit out.
+      const int nb = n0 < n1 ? n0 : n1;
+      int j = 0;
+      for (; j + 1 < nb; ++j) {
         const int gj = gt + j;
         const int st = gj % NS;
-        const bool more = j + 1 < n;
         const int st1 = (gj + 1) % NS;
-        const bool last_s = j + 2 == n;  // S(j+1) is this item's last S MMA
         if (!kOneKV && !warp_wait(smem_u32(&bar_v[st]), (gj / NS) & 1, abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
-        // warpgroup 0
-        if (!warp_wait(smem_u32(&bar_p[0]), gj & 1, abort_flag, p.dev_status)) {
+        if (!warp_wait(smem_u32(&bar_p[0]), (g0 + j) & 1, abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         issue_pv<D>(O_t[0], S_t[0], vd[st], j > 0, e);
-        if (more) {
-          if (!warp_wait(smem_u32(&bar_k[st1]), ((gj + 1) / NS) & 1, abort_flag, p.dev_status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
-          mma_commit_elect(smem_u32(&bar_s[0]), e);
-          if (last_s) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
-        } else {
-          mma_commit_elect(smem_u32(&bar_o[0]), e);
+        if (!warp_wait(smem_u32(&bar_k[st1]), ((gj + 1) / NS) & 1, abort_flag, p.dev_status)) {
+          ok = false;
+          break;
         }
-        // warpgroup 1
-        if (!warp_wait(smem_u32(&bar_p[1]), gj & 1, abort_flag, p.dev_status)) {
+        tc_fence_after();
+        issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
+        mma_commit_elect(smem_u32(&bar_s[0]), e);
+        if (j + 2 == n0) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
+        if (!warp_wait(smem_u32(&bar_p[1]), (g1 + j) & 1, abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         issue_pv<D>(O_t[1], S_t[1], vd[st], j > 0, e);
         mma_commit_elect(smem_u32(&bar_kv_empty[st]), e);
-        if (more) {
-          issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
-          mma_commit_elect(smem_u32(&bar_s[1]), e);
-          if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
-          if (last_s) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
-        } else {
-          mma_commit_elect(smem_u32(&bar_o[1]), e);
+        issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
+        mma_commit_elect(smem_u32(&bar_s[1]), e);
+        if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
+        if (j + 2 == n1) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
+      }
+      for (; ok && j < n; ++j) {
+        const int gj = gt + j;
+        const int st = gj % NS;
+        const int st1 = (gj + 1) % NS;
+        const bool act0 = j < n0, act1 = j < n1;
+        const bool more0 = j + 1 < n0, more1 = j + 1 < n1;
+        if (!kOneKV && !warp_wait(smem_u32(&bar_v[st]), (gj / NS) & 1, abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
+        // warpgroup 0
+        if (act0) {
+          if (!warp_wait(smem_u32(&bar_p[0]), (g0 + j) & 1, abort_flag, p.dev_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv<D>(O_t[0], S_t[0], vd[st], j > 0, e);
+          if (more0) {
+            if (!warp_wait(smem_u32(&bar_k[st1]), ((gj + 1) / NS) & 1, abort_flag,
+                           p.dev_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
+            mma_commit_elect(smem_u32(&bar_s[0]), e);
+            if (!kOneKV && !more1) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
+            if (j + 2 == n0) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
+          } else {
+            mma_commit_elect(smem_u32(&bar_o[0]), e);
+          }
+        }
+        // warpgroup 1
+        if (act1) {
+          if (!warp_wait(smem_u32(&bar_p[1]), (g1 + j) & 1, abort_flag, p.dev_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv<D>(O_t[1], S_t[1], vd[st], j > 0, e);
+        }
+        mma_commit_elect(smem_u32(&bar_kv_empty[st]), e);  // every PV of this tile issued
+        if (act1) {
+          if (more1) {
+            if (!more0 && !warp_wait(smem_u32(&bar_k[st1]), ((gj + 1) / NS) & 1, abort_flag,
+                                     p.dev_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
+            mma_commit_elect(smem_u32(&bar_s[1]), e);
+            if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
+            if (j + 2 == n1) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
+          } else {
+            mma_commit_elect(smem_u32(&bar_o[1]), e);
+          }
         }
       }
       gt += n;
+      g0 += n0;
+      g1 += n1;
       ++nq;
     }
     // Drain: every MMA issued by this warp is complete before TMEM is freed.
@@ -465,7 +533,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       Item w;
       bool bad;
       decode_item(p, it, w, &bad);
-      const int n_tiles = w.n_tiles;
+      const int n_tiles = wg == 0 ? w.n0 : w.n1;  // tiles this warpgroup's rows can see
       const int64_t Lq = w.Lq, Lk = w.Lk;
       const int64_t i = w.q_lo + wg * kBlockM + row;  // query row within the sequence
       int64_t limit = Lk;                            // keys [0, limit) visible to this row
