@@ -88,13 +88,31 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// TMA store of one box from shared memory, tracked as a bulk group of this thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every bulk group of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ int kslab_of(int r, int i) {  // i-th K-only slab (global id)
   return r == 0 ? 4 + i : (i < 4 ? i : 8);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap kvmap, const SparseParams p) {
+                       const __grid_constant__ CUtensorMap kvmap,
+                       const __grid_constant__ CUtensorMap outmap, const SparseParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_qhi, bar_qlo_smem, bar_qlo, bar_kfull[2], bar_vfull[2], bar_kempty[2],
       bar_vempty[2], bar_s[2], bar_p[2], bar_o, bar_drain;
@@ -533,21 +551,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- epilogue: out = O / l (or a part's O, to its slot), by all 16 warps ----
   // Warp w reads TMEM lanes 32(w&3)..+31 (its heads) and columns 64(w>>2)..+63 of the
-  // O half; a 4 KB slice of the idle gather stages per warp turns each head's values
-  // into 128-byte segments, four heads per store.
+  // O half, 32 columns at a time, into an 8 KB slice of the idle gather stages laid out
+  // as two 128-byte-swizzled 32 x 32 boxes; whole rows go out by TMA stores (a part's
+  // O goes to its slot with plain stores, four heads per instruction).
   const bool fine = *abort_flag == 0;  // stable: every role has finished
   if (fine) {
     const int hq = warp & 3;
-    float4* stage = reinterpret_cast<float4*>(smem + kQhiBytes + warp * 4096);
     const uint32_t O_row = tmem + 256 + (static_cast<uint32_t>(hq * 32) << 16);
     const float inv_l = s_inv_l[hq * 32 + lane];
-    const int64_t ostride = nparts == 1 ? kDv : 256;
-    float* obase =
-        nparts == 1
-            ? p.out + ((int64_t)n * kHeads + hq * 32) * kDv + 256 * r
-            : p.partial + (int64_t)((u - p.n_main) * nparts + part) * kSlotFloats + hq * 32 * 256;
+    float* slot = p.partial + (int64_t)((u - p.n_main) * nparts + part) * kSlotFloats +
+                  hq * 32 * 256;
 #pragma unroll 1
-    for (int c0 = (warp >> 2) * 64; c0 < (warp >> 2) * 64 + 64; c0 += 32) {
+    for (int ci = 0; ci < 2; ++ci) {
+      const int c0 = (warp >> 2) * 64 + 32 * ci;
+      float4* stage = reinterpret_cast<float4*>(smem + kQhiBytes + warp * 8192 + ci * 4096);
       uint32_t o[32];
       if (nt > 0) {
         tmem_ld32(O_row + c0, o);
@@ -562,15 +579,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
                         __uint_as_float(o[4 * q + 2]) * inv_l,
                         __uint_as_float(o[4 * q + 3]) * inv_l);
-      __syncwarp();
+      if (nparts == 1) {
+        fence_proxy_async_smem();  // the staged rows, for the copy engine
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&outmap, smem_u32(stage), 256 * r + c0, hq * 32, n);
+          bulk_commit();
+        }
+      } else {
+        __syncwarp();
 #pragma unroll
-      for (int rr = 0; rr < 32; rr += 4) {
-        const int hh = rr + (lane >> 3), q = lane & 7;
-        *reinterpret_cast<float4*>(obase + (int64_t)hh * ostride + c0 + 4 * q) =
-            stage[hh * 8 + (q ^ (hh & 7))];
+        for (int rr = 0; rr < 32; rr += 4) {
+          const int hh = rr + (lane >> 3), q = lane & 7;
+          *reinterpret_cast<float4*>(slot + (int64_t)hh * 256 + c0 + 4 * q) =
+              stage[hh * 8 + (q ^ (hh & 7))];
+        }
       }
-      __syncwarp();
     }
+    if (nparts == 1 && lane == 0) bulk_wait_read_all();  // the slices stay until read
   }
   if (nparts > 1 && fine) {
     // The last part of the unit to finish merges all parts in part order:
@@ -689,6 +715,17 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
     *drv_err = (int)rr;
     return cudaErrorInvalidValue;
   }
+  // The output as 32 x 32 fp32 boxes (32 columns = 128 bytes, 32 heads) for TMA stores.
+  CUtensorMap outmap;
+  const uint64_t o_dims[3] = {(uint64_t)kDv, (uint64_t)kHeads, (uint64_t)a.nq};
+  const uint64_t o_strides[2] = {(uint64_t)kDv * 4, (uint64_t)kHeads * kDv * 4};
+  const uint32_t o_box[3] = {32, 32, 1};
+  rr = encode_tensor_map(&outmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.out, o_dims, o_strides,
+                         o_box, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rr != CUDA_SUCCESS) {
+    *drv_err = (int)rr;
+    return cudaErrorInvalidValue;
+  }
   SparseParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.kv = static_cast<const uint16_t*>(a.kv_cache);
@@ -736,7 +773,7 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kvmap, p);
+  sparse_attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kvmap, outmap, p);
   return cudaGetLastError();
 }
 
