@@ -112,7 +112,11 @@ def test_full_varlen_config_sampled_rows(tts):
     g = np.random.default_rng(45)
     T = int(inp.cu_seqlens_q[-1])
     tok = g.integers(0, T, 512).astype(np.int32)
-    tok[:len(inp.cu_seqlens_q) - 1] = inp.cu_seqlens_q[:-1].numpy()  # every sequence's row 0
+    cu = inp.cu_seqlens_q.numpy()
+    nb = len(cu) - 1
+    tok[:nb] = cu[:-1]  # every sequence's row 0
+    tok[nb:2 * nb] = cu[1:] - 1  # and its last row (last query tile, causal diagonal)
+    tok[2 * nb:3 * nb] = np.minimum(cu[:-1] + 128, cu[1:] - 1)  # the second query tile's first
     head = g.integers(0, 32, 512).astype(np.int32)
     ro, rl = oracle_full(inp, rows=(tok, head))
     assert_close_attn(out[tok, head].cpu().numpy(), ro, "varlen sampled")
