@@ -22,10 +22,12 @@
 //   * warps 0-3 gather the K-only slabs (16-byte cp.async into the 128-byte-swizzled
 //     layout the MMA reads), warps 4-7 the V slabs (TMA tile::gather4, four rows per
 //     copy, same layout), warp 8 issues MMAs, warps 12-15 run the softmax (one head
-//     per thread); all 16 warps write the output.
-// Both CTAs of a query compute the same S and the same softmax bits; each
-// accumulates O for its 256 V columns (the S work is done twice so that no
-// partial scores have to be exchanged between SMs).
+//     per thread); all 16 warps write the output (TMA stores of staged boxes).
+// Both CTAs of a query compute all of S (each over the 9 slabs in its own fixed
+// order, so their roundings may differ) and accumulate O for their 256 V columns:
+// the S work is done twice so that no partial scores move between SMs. The (query,
+// half) units of the last, partial wave of CTAs can run as 2-4 parts over
+// consecutive tiles of the sorted list, merged in part order by the last to finish.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_qlo));  // also: the V stages are free for gathering
     } else {
-      go = mbar_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status);
+      go = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_qlo), 0, abort_flag, p.dev_status));
     }
     const bool kside = warp < 4;
     // Producer warp w of a role copies entries 16*(w&3) .. +15 of the tile. K side: lane
@@ -348,9 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int chunk = lane & 7;
     for (int j = 0; go && j < nt; ++j) {
       const int st = j & 1;
-      if (j >= 2) {
+      if (j >= 2) {  // the decision is warp-wide: the shuffles below need every lane
         const uint32_t eb = smem_u32(kside ? &bar_kempty[st] : &bar_vempty[st]);
-        if (!mbar_wait(eb, ((j >> 1) - 1) & 1, abort_flag, p.dev_status)) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(eb, ((j >> 1) - 1) & 1, abort_flag, p.dev_status)))
+          break;
       }
       const int32_t mine = rows_q[0];
       const int src = (j & 1) * 16;  // the lanes that hold this tile's rows
