@@ -150,12 +150,17 @@ __device__ __forceinline__ bool decode_item(const AttnParams& p, int it, Item& w
     *bad = (pr == 0 && h == 0);  // report each bad sequence once
     return false;
   }
-  const int64_t q_lo = (int64_t)pr * 2 * kBlockM;  // first query row (within the sequence)
+  // First query row of the pair (within the sequence). With an odd number of 128-row
+  // query tiles the pairs start one tile early, so the tile without a partner is tile 0
+  // (the cheapest under a causal mask: one key tile) and the first warpgroup of pair 0
+  // has no rows.
+  const int64_t n_qt = (Lq + kBlockM - 1) / kBlockM;
+  const int64_t q_lo = (int64_t)pr * 2 * kBlockM - ((n_qt & 1) ? kBlockM : 0);
   if (q_lo >= Lq) return false;
   // Keys each warpgroup's rows can see: all of them, or (causal) up to its last row's
   // diagonal; none for a warpgroup without rows (the odd last tile of a sequence).
   auto keys_for = [&](int64_t r_first, int64_t r_end) -> int64_t {
-    if (r_first >= Lq) return 0;
+    if (r_first >= Lq || r_end <= 0) return 0;
     if (!p.causal) return Lk;
     const int64_t lim = (r_end < Lq ? r_end : Lq) - 1 + (Lk - Lq) + 1;
     return lim < 0 ? 0 : (lim < Lk ? lim : Lk);
@@ -635,13 +640,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const int r = rr + lane / lpr, q = lane % lpr;
           const float4 v = stage[r * 8 + (q ^ (r & 7))];
           const int64_t ii = row0 + r;
-          if (ii < Lq)
+          if (ii >= 0 && ii < Lq)
             *reinterpret_cast<float4*>(p.out + ((w.q_start + ii) * p.hq + w.h) * (int64_t)D +
                                        c0 + 4 * q) = v;
         }
         __syncwarp();
       }
-      if (i < Lq && p.lse != nullptr)
+      if (i >= 0 && i < Lq && p.lse != nullptr)
         p.lse[(w.q_start + i) * p.hq + w.h] =
             (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
       gt += n_tiles;
