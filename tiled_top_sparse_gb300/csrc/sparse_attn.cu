@@ -90,23 +90,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// TMA store of one box from shared memory, tracked as a bulk group of this thread.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1,
-                                             int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until every bulk group of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 __device__ __forceinline__ int kslab_of(int r, int i) {  // i-th K-only slab (global id)
   return r == 0 ? 4 + i : (i < 4 ? i : 8);
 }
