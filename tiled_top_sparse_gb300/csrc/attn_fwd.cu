@@ -580,11 +580,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           m_ref = m_new;
         }
         const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
-        // P packed as bf16 pairs over sr[0..63], in place.
-        l += exp2_pack_sum<128>(sr, c, neg_mc);
+        // P packed as bf16 pairs in place (over sr[0..63], or sr[0..31] and sr[64..95]).
+        if constexpr (D >= 128) {
+          // Two halves: the first half of P goes to TMEM while the second is computed
+          // (and fewer values stay live, which at d = 128 removes most spills).
+          const float l_a = exp2_pack_sum<64>(sr, c, neg_mc);
+          tmem_st32(S_row, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+          const float l_b = exp2_pack_sum<64>(sr + 64, c, neg_mc);
+          tmem_st32(S_row + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[64]));
+          l += l_a + l_b;
+        } else {
+          l += exp2_pack_sum<128>(sr, c, neg_mc);
   #pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4)
-          tmem_st32(S_row + q4 * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[q4 * 32]));
+          for (int q4 = 0; q4 < 2; ++q4)
+            tmem_st32(S_row + q4 * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[q4 * 32]));
+        }
         // Rescale O (its previous PV finished: it was issued before this tile's S MMA,
         // whose completion this thread observed).
         if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
