@@ -347,6 +347,48 @@ def topk_protocol(step, dev, peaks):
             "scaled_frac_hbm": gbs_big / peaks["hbm_gbs"]}
 
 
+def topk_long_protocol(step, dev, peaks):
+    """Long-row top-k (rows split over many CTAs), outside the step: the last 64 query
+    rows of a 262144-token context, k = 2048. A CUDA graph of 16 calls rotating over 4
+    input sets (256 MB, > L2, so every call reads its rows from HBM); graph time / calls.
+    The indices of every set are checked against the first set's."""
+    t = step.tts
+    inp = W.topk_long_inputs()
+    rows, cols = inp.logits.shape
+    k = inp.k
+    lg = inp.logits.to(dev)
+    rs, rl = inp.row_starts.to(dev), inp.row_lens.to(dev)
+    sets = [(lg.clone() if i else lg, torch.empty((rows, k), dtype=torch.int32, device=dev))
+            for i in range(4)]
+    ws = torch.empty(t.topk_long_workspace_bytes(rows, cols, k), dtype=torch.uint8, device=dev)
+    n_call = 16
+    s = torch.cuda.Stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for x, o in sets:
+            t.topk_select_long(x, rs, rl, k, idx=o, workspace=ws, status=step.status)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n_call):
+                x, o = sets[i % len(sets)]
+                t.topk_select_long(x, rs, rl, k, idx=o, workspace=ws, status=step.status)
+        g.replay()
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n_call
+    for _, o in sets:
+        assert torch.equal(o, sets[0][1]), "long top-k: input sets disagree"
+    nbytes = int(inp.row_lens.sum().item()) * 4 + rows * k * 4 + rows * 8
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del sets, ws, lg
+    return {"workload": f"{rows} rows x {cols} (last queries of a {cols}-token context), k {k}",
+            "us_per_call": us, "launches_per_call": 7, "bytes": nbytes, "gbs": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"],
+            "protocol": f"CUDA graph of {n_call} calls over 4 rotating input sets"}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(n_rows: int = 192, n_queries: int = 8):
     """Time the float64 oracle on bounded samples of each part.
@@ -536,6 +578,7 @@ def run_gpu(args, rank, world, local):
         comp[p] = c
     if "topk" in parts and rank == 0:
         comp["topk"].update(topk_protocol(step, dev, peaks))
+        comp["topk_long"] = topk_long_protocol(step, dev, peaks)
         tts.check_status(step.status, "bench top-k protocol")
     dom = max(parts, key=lambda p: comp[p]["ms"])
     dc = comp[dom]

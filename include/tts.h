@@ -130,6 +130,28 @@ tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows
                            int32_t* idx, uint32_t* dev_status, void* stream);
 
 /*
+ * Top-k over long rows: the same result as tts_topk_select (same definition,
+ * tie rule and output layout, see above) for rows of any length up to 2^30,
+ * such as the long-context indexer rows of "从 SGLang Kernel源码到 GPU Trace"
+ * (section 2.2). Each row is split over many CTAs: three histogram passes of a
+ * radix select (integer atomics only), a collect pass that ranks ties by
+ * position, and a per-row sort of the k picks, so the result is deterministic.
+ *
+ * workspace  device scratch of at least tts_topk_long_workspace_bytes(rows,
+ *            row_stride, k) bytes, 16-byte aligned, owned by the caller and
+ *            not shared by two calls in flight; its contents are overwritten
+ *            (the call zeroes what it needs on the stream first).
+ * Limits: 1 <= k <= 4096, 1 <= row_stride <= 2^30 (TTS_ERR_UNSUPPORTED
+ * otherwise); a too small or misaligned workspace is TTS_ERR_INVALID_ARG.
+ * Errors in row_starts / row_lens behave as in tts_topk_select.
+ */
+size_t tts_topk_long_workspace_bytes(int32_t rows, int64_t row_stride, int32_t k);
+tts_status tts_topk_select_long(const float* logits, int64_t row_stride, int32_t rows,
+                                const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                                int32_t* idx, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_status, void* stream);
+
+/*
  * Sparse attention over a paged KV cache, invariant to the order of the index list.
  *
  * Follows "推理引擎的蝴蝶效应 -- 从V32 模型的输出不一致说起" (section 实验方法和

@@ -70,6 +70,26 @@ def test_topk_host_validation(L):
     assert f(P, 10, 0, P, P, 4, P, NUL, NUL) == tts.TTS_OK  # nothing to do
 
 
+def test_topk_long_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    f = L.tts_topk_select_long
+    need = L.tts_topk_long_workspace_bytes(3, 300000, 2048)
+    # 19 chunks of 16384 per row: histograms, counters, chunk histograms and 2048 picks
+    assert need >= 3 * 4 * (2 * 4096 + 256 + 4 + 19 * 256 + 2 * 2048)
+    assert L.tts_topk_long_workspace_bytes(0, 300000, 2048) == 0
+    assert L.tts_topk_long_workspace_bytes(3, 300000, 4097) == 0
+    A = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced
+    assert f(NUL, 300000, 3, P, P, 2048, P, A, need, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 300000, 3, P, P, 0, P, A, need, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 300000, 3, P, P, 4097, P, A, need, NUL, NUL) == tts.TTS_ERR_UNSUPPORTED
+    assert f(P, (1 << 30) + 1, 3, P, P, 16, P, A, need, NUL, NUL) == tts.TTS_ERR_UNSUPPORTED
+    assert f(P, 300000, 3, P, P, 2048, P, NUL, need, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 300000, 3, P, P, 2048, P, A, need - 1, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(P, 300000, 3, P, P, 2048, P, ctypes.c_void_p(0x10008), need, NUL,
+             NUL) == tts.TTS_ERR_INVALID_ARG  # misaligned workspace
+    assert f(P, 300000, 0, P, P, 2048, P, NUL, 0, NUL, NUL) == tts.TTS_OK  # nothing to do
+
+
 def _attn(L, **kw):
     a = dict(q=P, k=P, v=P, dt=0, tq=256, tk=256, cq=P, ck=P, b=1, mq=256, mk=256, hq=2, hkv=1,
              d=64, causal=0, scale=0.125, out=P, lse=NUL, ws=NUL, wsb=0, st=NUL, stream=NUL)

@@ -44,6 +44,8 @@ EXPORTED = (
     "tts_attn_workspace_bytes",
     "tts_attn_fwd_varlen",
     "tts_topk_select",
+    "tts_topk_long_workspace_bytes",
+    "tts_topk_select_long",
     "tts_sparse_attn_paged",
     "tts_sparse_workspace_bytes",
     "tts_attn_fwd_varlen_f32_noalloc",
@@ -82,6 +84,10 @@ def lib() -> ctypes.CDLL:
     L.tts_attn_fwd_varlen.restype = ctypes.c_int
     L.tts_topk_select.argtypes = [P, i64, i32, P, P, i32, P, P, P]
     L.tts_topk_select.restype = ctypes.c_int
+    L.tts_topk_long_workspace_bytes.argtypes = [i32, i64, i32]
+    L.tts_topk_long_workspace_bytes.restype = ctypes.c_size_t
+    L.tts_topk_select_long.argtypes = [P, i64, i32, P, P, i32, P, P, ctypes.c_size_t, P, P]
+    L.tts_topk_select_long.restype = ctypes.c_int
     L.tts_sparse_attn_paged.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, i32, i32, P, i32,
                                         f32, P, P, P, ctypes.c_size_t, P, P]
     L.tts_sparse_attn_paged.restype = ctypes.c_int
@@ -200,6 +206,35 @@ def topk_select(logits, row_starts, row_lens, k, idx=None, status=None):
     code = lib().tts_topk_select(_ptr(logits), stride, rows, _ptr(row_starts), _ptr(row_lens),
                                  int(k), _ptr(idx), _ptr(status), _stream(logits.device))
     _check(code, "tts_topk_select")
+    return idx
+
+
+def topk_long_workspace_bytes(rows, row_stride, k) -> int:
+    return int(lib().tts_topk_long_workspace_bytes(int(rows), int(row_stride), int(k)))
+
+
+def topk_select_long(logits, row_starts, row_lens, k, idx=None, workspace=None, status=None):
+    """Deterministic top-k over long rows (tts_topk_select_long): the same result as
+    topk_select for rows up to 2^30 values. Returns idx int32 [rows, k]. A workspace of
+    topk_long_workspace_bytes(...) bytes is allocated here when `workspace` is missing."""
+    _cuda_contig(logits, "logits", torch.float32)
+    _need(logits.dim() == 2, "logits must be [rows, row_stride]")
+    _cuda_contig(row_starts, "row_starts", torch.int32)
+    _cuda_contig(row_lens, "row_lens", torch.int32)
+    rows, stride = logits.shape
+    _need(row_starts.numel() == rows and row_lens.numel() == rows, "row_starts/row_lens size")
+    if idx is None:
+        idx = torch.empty((rows, int(k)), dtype=torch.int32, device=logits.device)
+    _cuda_contig(idx, "idx", torch.int32)
+    _need(tuple(idx.shape) == (rows, int(k)), "idx shape")
+    need = topk_long_workspace_bytes(rows, stride, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=logits.device)
+    _cuda_contig(workspace, "workspace", torch.uint8)
+    code = lib().tts_topk_select_long(_ptr(logits), stride, rows, _ptr(row_starts),
+                                      _ptr(row_lens), int(k), _ptr(idx), _ptr(workspace),
+                                      workspace.numel(), _ptr(status), _stream(logits.device))
+    _check(code, "tts_topk_select_long")
     return idx
 
 

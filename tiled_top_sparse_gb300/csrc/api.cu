@@ -179,6 +179,28 @@ tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows
                                       dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+size_t tts_topk_long_workspace_bytes(int32_t rows, int64_t row_stride, int32_t k) {
+  if (rows <= 0 || row_stride < 1 || k < 1 || k > 4096 || row_stride > (int64_t(1) << 30))
+    return 0;
+  return topk_long_workspace_bytes(rows, row_stride, k);
+}
+
+tts_status tts_topk_select_long(const float* logits, int64_t row_stride, int32_t rows,
+                                const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                                int32_t* idx, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_status, void* stream) {
+  if (logits == nullptr || row_starts == nullptr || row_lens == nullptr || idx == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (rows < 0 || row_stride < 1 || k < 1) return TTS_ERR_INVALID_ARG;
+  if (k > 4096 || row_stride > (int64_t(1) << 30)) return TTS_ERR_UNSUPPORTED;
+  if (rows == 0) return TTS_OK;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 15) != 0 ||
+      workspace_bytes < topk_long_workspace_bytes(rows, row_stride, k))
+    return TTS_ERR_INVALID_ARG;
+  return from_cuda(launch_topk_long(logits, row_stride, rows, row_starts, row_lens, k, idx,
+                                    workspace, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 size_t tts_sparse_workspace_bytes(int32_t nq) {
   if (nq <= 0) return 0;
   int dev = 0, sms = 0;

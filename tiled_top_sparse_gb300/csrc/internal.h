@@ -12,6 +12,11 @@ size_t topk_smem_bytes(int64_t row_stride, int k);
 cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t rows,
                                const int32_t* row_starts, const int32_t* row_lens, int32_t k,
                                int32_t* idx, uint32_t* dev_status, cudaStream_t stream);
+size_t topk_long_workspace_bytes(int32_t rows, int64_t row_stride, int32_t k);
+cudaError_t launch_topk_long(const float* logits, int64_t row_stride, int32_t rows,
+                             const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                             int32_t* idx, void* workspace, uint32_t* dev_status,
+                             cudaStream_t stream);
 
 // ---- dense attention
 struct AttnArgs {

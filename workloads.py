@@ -27,7 +27,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-SEEDS = {"tiny": 0, "vision": 1, "varlen": 2, "topk": 3, "sparse": 4}
+SEEDS = {"tiny": 0, "vision": 1, "varlen": 2, "topk": 3, "sparse": 4, "topk_long": 5}
 PERM_SEEDS = tuple(range(100, 108))
 
 
@@ -145,6 +145,13 @@ def topk_inputs(rows=323, cols=2590, k=2048, seed=None, causal=True, bf16_grid=T
         row_starts = torch.zeros(rows, dtype=torch.int32)
     return TopkInputs(x, torch.as_tensor(row_starts, dtype=torch.int32),
                       torch.as_tensor(row_lens, dtype=torch.int32), int(k))
+
+
+def topk_long_inputs(rows=64, cols=262144, k=2048, seed=None) -> TopkInputs:
+    """Indexer logits of the last `rows` queries of a `cols`-token context (rows longer
+    than one CTA can hold: the long-row top-k); same value recipe as topk_inputs."""
+    return topk_inputs(rows=rows, cols=cols, k=k,
+                       seed=SEEDS["topk_long"] if seed is None else seed, causal=True)
 
 
 @dataclass
