@@ -389,6 +389,64 @@ def topk_long_protocol(step, dev, peaks):
             "protocol": f"CUDA graph of {n_call} calls over 4 rotating input sets"}
 
 
+def decode_protocol(step, dev, peaks):
+    """Decode-shaped sparse attention outside the step: 64 requests, each with a
+    32768-token context (the paged cache's max_seq_len on p3) in its own shuffled pages of
+    64, one query, 2048 indices; then each request's next KV row is written through its
+    page table. The 2.4 GB KV pool and the queries come from a seeded device generator
+    (values do not affect the timing); page tables and index lists as in
+    workloads.sparse_decode_inputs. Two index sets alternate (302 MB of gathered rows,
+    > L2); 20 calls timed with CUDA events."""
+    t = step.tts
+    nreq, ctx, ps, topk, dqk, dv = 64, 32768, 64, 2048, 576, 512
+    g = torch.Generator(device="cpu").manual_seed(W.SEEDS["decode"])
+    per = ctx // ps + 1
+    pool = nreq * per
+    tables = torch.randperm(pool, generator=g).to(torch.int32).view(nreq, per).to(dev)
+    lens = torch.full((nreq,), ctx, dtype=torch.int32, device=dev)
+    idx_sets = [torch.stack([torch.randperm(ctx, generator=g)[:topk] for _ in range(nreq)])
+                .to(torch.int32).to(dev) for _ in range(2)]
+    gd = torch.Generator(device=dev).manual_seed(W.SEEDS["decode"])
+    kv = torch.randn(pool, ps, dqk, generator=gd, device=dev).to(torch.bfloat16)
+    q = torch.randn(nreq, 128, dqk, generator=gd, device=dev).to(torch.bfloat16)
+    kv_new = torch.randn(nreq, dqk, generator=gd, device=dev).to(torch.bfloat16)
+    out = torch.empty((nreq, 128, dv), dtype=torch.float32, device=dev)
+    lse = torch.empty((nreq, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(t.sparse_workspace_bytes(nreq), 16), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(dqk)
+    call = lambda i: t.sparse_attn_decode(q, kv, tables, lens, idx_sets[i % 2], scale, dv=dv,
+                                          out=out, lse=lse, workspace=ws, status=step.status)
+    s = torch.cuda.Stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def graph_us(fn, n):
+        with torch.cuda.stream(s):
+            for i in range(4):
+                fn(i)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                for i in range(n):
+                    fn(i)
+            gr.replay()
+            e0.record(s)
+            gr.replay()
+            e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    us = graph_us(call, 20)
+    us_w = graph_us(lambda i: t.paged_kv_write(kv, tables, kv_new, lens, status=step.status), 20)
+    gathered = nreq * topk * dqk * 2
+    flops = 2.0 * 128 * nreq * topk * (dqk + dv)
+    gbs = gathered / (us * 1e-6) / 1e9
+    del kv, q, ws, idx_sets
+    return {"workload": f"{nreq} requests x {ctx}-token contexts (pages of {ps}), "
+                        f"128 heads, {topk} indices", "us_per_call": us,
+            "gathered_bytes": gathered, "gathered_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+            "tflops": flops / (us * 1e-6) / 1e12, "kv_write_us": us_w,
+            "protocol": "CUDA graph of 20 calls, two alternating index sets (302 MB gathered)"}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(n_rows: int = 192, n_queries: int = 8):
     """Time the float64 oracle on bounded samples of each part.
@@ -579,6 +637,9 @@ def run_gpu(args, rank, world, local):
     if "topk" in parts and rank == 0:
         comp["topk"].update(topk_protocol(step, dev, peaks))
         comp["topk_long"] = topk_long_protocol(step, dev, peaks)
+    if "sparse" in parts and rank == 0:
+        comp["sparse_decode"] = decode_protocol(step, dev, peaks)
+        tts.check_status(step.status, "bench decode protocol")
         tts.check_status(step.status, "bench top-k protocol")
     dom = max(parts, key=lambda p: comp[p]["ms"])
     dc = comp[dom]

@@ -195,6 +195,58 @@ tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, i
                                  void* stream);
 
 /*
+ * Decode-shaped sparse attention: one query per request, each request with its own
+ * page table and length, in one call. The same computation as tts_sparse_attn_paged
+ * (see above: sorted index list, so bitwise invariant under index permutations),
+ * with query n reading its KV rows through page_tables[n, :] and its own kv_lens[n]:
+ * the per-request page tables of the paged cache in "从 SGLang Kernel源码到 GPU
+ * Trace" (section 2.2, PagedKVCache) under the sparse attention and index rule of
+ * "推理引擎的蝴蝶效应" (sections 实验方法和结果, 进一步探索). With few requests, the
+ * workspace lets every (request, V half) unit run as 2 or 4 CTAs over consecutive
+ * tiles of its sorted list, merged in part order (split-KV with a fixed-order combine).
+ *
+ * q           device bf16 [nreq, num_heads, dqk]
+ * kv_cache    device bf16 [num_pages, page_size, dqk], shared by all requests
+ * page_tables device int32 [nreq, max_pages]; entry g of row n = physical page of
+ *             request n's logical page g
+ * kv_lens     device int32 [nreq]; a negative length reads as 0 and is reported
+ * idx         device int32 [nreq, topk], logical positions in the request's sequence
+ * out, lse, workspace, dev_status, errors and built shape: as tts_sparse_attn_paged
+ * (the workspace size is tts_sparse_workspace_bytes(nreq)); max_pages >= 1.
+ */
+tts_status tts_sparse_attn_decode(const void* q, int32_t nreq, int32_t num_heads, int32_t dqk,
+                                  int32_t dv, const void* kv_cache, int32_t num_pages,
+                                  int32_t page_size, const int32_t* page_tables,
+                                  int32_t max_pages, const int32_t* kv_lens, const int32_t* idx,
+                                  int32_t topk, float scale, float* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                  void* stream);
+
+/*
+ * Paged KV cache write: the write path of the cache read above ("推理引擎的蝴蝶效应",
+ * section 实验方法和结果, where the cache is reached through pagetable_1 and its write
+ * path is ruled out; "从 SGLang Kernel源码到 GPU Trace", section 2.2, PagedKVCache).
+ * Token t (of ntok) belongs to request req_ids[t] (req_ids NULL: request t) at logical
+ * position positions[t]; its row kv_new[t, :] is copied to
+ *   kv_cache[page_tables[req, pos / page_size], pos % page_size, :].
+ * A token whose request is outside [0, nreq), whose position is outside
+ * [0, max_pages * page_size) or whose page entry is outside [0, num_pages) is skipped
+ * and sets TTS_DEV_INDEX_RANGE. Two tokens of one call with the same destination: the
+ * row left there is one of theirs, which one is unspecified.
+ *
+ * kv_new      device bf16 [ntok, dim], dim a multiple of 8
+ * req_ids     device int32 [ntok] or NULL;  positions device int32 [ntok]
+ * page_tables device int32 [nreq, max_pages]
+ * kv_cache    device bf16 [num_pages, page_size, dim]
+ * kv_new and kv_cache 16-byte aligned; nothing is allocated.
+ */
+tts_status tts_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
+                              const int32_t* req_ids, const int32_t* positions,
+                              const int32_t* page_tables, int32_t max_pages, int32_t nreq,
+                              void* kv_cache, int32_t num_pages, int32_t page_size,
+                              uint32_t* dev_status, void* stream);
+
+/*
  * Workspace bytes that let tts_sparse_attn_paged split the last wave of nq queries on
  * the current device (0: no split for this shape, or no device). At most about
  * 132 KB per SM.

@@ -136,6 +136,36 @@ def test_sparse_host_validation(L):
     assert _sparse(L, nq=0) == tts.TTS_OK
 
 
+def test_decode_and_kv_write_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    f = L.tts_sparse_attn_decode
+    F32 = ctypes.c_float
+
+    def dec(**kw):
+        a = dict(q=P, n=4, h=128, dqk=576, dv=512, kv=P, pages=64, ps=64, pt=P, maxp=8, lens=P,
+                 idx=P, topk=2048, scale=F32(0.05), out=P, lse=NUL, ws=NUL, wsb=0, st=NUL,
+                 stream=NUL)
+        a.update(kw)
+        return f(*a.values())
+    assert dec(lens=NUL) == tts.TTS_ERR_INVALID_ARG           # kv_lens is required
+    assert dec(pt=NUL) == tts.TTS_ERR_INVALID_ARG
+    assert dec(maxp=0) == tts.TTS_ERR_INVALID_ARG
+    assert dec(scale=F32(0.0)) == tts.TTS_ERR_INVALID_ARG
+    assert dec(h=64) == tts.TTS_ERR_UNSUPPORTED
+    assert dec(topk=2049) == tts.TTS_ERR_UNSUPPORTED
+    assert dec(q=ctypes.c_void_p(0x1008)) == tts.TTS_ERR_INVALID_ARG  # misaligned
+    assert dec(n=0) == tts.TTS_OK
+    g = L.tts_paged_kv_write
+    #        kv_new ntok dim req pos  pt maxp nreq cache pages ps st stream
+    assert g(NUL, 4, 576, NUL, P, P, 8, 4, P, 64, 64, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert g(P, 4, 577, NUL, P, P, 8, 4, P, 64, 64, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert g(P, 4, 576, NUL, NUL, P, 8, 4, P, 64, 64, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert g(P, 4, 576, NUL, P, P, 0, 4, P, 64, 64, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert g(ctypes.c_void_p(0x1004), 4, 576, NUL, P, P, 8, 4, P, 64, 64, NUL,
+             NUL) == tts.TTS_ERR_INVALID_ARG
+    assert g(P, 0, 576, NUL, P, P, 8, 4, P, 64, 64, NUL, NUL) == tts.TTS_OK
+
+
 def test_sparse_workspace_bytes_without_device(L):
     # No GPU here: no split is planned; with nq <= 0 never.
     import torch

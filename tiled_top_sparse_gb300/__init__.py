@@ -48,6 +48,8 @@ EXPORTED = (
     "tts_topk_select_long",
     "tts_sparse_attn_paged",
     "tts_sparse_workspace_bytes",
+    "tts_sparse_attn_decode",
+    "tts_paged_kv_write",
     "tts_attn_fwd_varlen_f32_noalloc",
     "tts_debug_wait_timeout",
 )
@@ -91,6 +93,11 @@ def lib() -> ctypes.CDLL:
     L.tts_sparse_attn_paged.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, i32, i32, P, i32,
                                         f32, P, P, P, ctypes.c_size_t, P, P]
     L.tts_sparse_attn_paged.restype = ctypes.c_int
+    L.tts_sparse_attn_decode.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, i32, P, P, i32,
+                                         f32, P, P, P, ctypes.c_size_t, P, P]
+    L.tts_sparse_attn_decode.restype = ctypes.c_int
+    L.tts_paged_kv_write.argtypes = [P, i64, i32, P, P, P, i32, i32, P, i32, i32, P, P]
+    L.tts_paged_kv_write.restype = ctypes.c_int
     L.tts_sparse_workspace_bytes.argtypes = [i32]
     L.tts_sparse_workspace_bytes.restype = ctypes.c_size_t
     L.tts_attn_fwd_varlen_f32_noalloc.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, i32,
@@ -236,6 +243,69 @@ def topk_select_long(logits, row_starts, row_lens, k, idx=None, workspace=None, 
                                       workspace.numel(), _ptr(status), _stream(logits.device))
     _check(code, "tts_topk_select_long")
     return idx
+
+
+def sparse_attn_decode(q, kv_cache, page_tables, kv_lens, idx, scale, dv=512, out=None,
+                       lse=None, workspace=None, status=None, want_lse=True, split=True):
+    """Decode-shaped sparse attention (tts_sparse_attn_decode): one query per request,
+    request n reading through page_tables[n] with length kv_lens[n].
+
+    q bf16 [nreq, H, dqk], kv_cache bf16 [pages, page_size, dqk], page_tables int32
+    [nreq, max_pages], kv_lens int32 [nreq], idx int32 [nreq, topk]. Returns (out fp32
+    [nreq, H, dv], lse fp32 [nreq, H]); `split` as in sparse_attn_paged."""
+    _cuda_contig(q, "q", torch.bfloat16)
+    _cuda_contig(kv_cache, "kv_cache", torch.bfloat16)
+    _cuda_contig(page_tables, "page_tables", torch.int32)
+    _cuda_contig(kv_lens, "kv_lens", torch.int32)
+    _cuda_contig(idx, "idx", torch.int32)
+    _need(q.dim() == 3 and kv_cache.dim() == 3 and idx.dim() == 2 and page_tables.dim() == 2,
+          "ranks")
+    nreq, H, dqk = q.shape
+    pages, page_size, dk2 = kv_cache.shape
+    _need(dk2 == dqk and idx.shape[0] == nreq and page_tables.shape[0] == nreq and
+          kv_lens.numel() == nreq, "shapes")
+    if out is None:
+        out = torch.empty((nreq, H, dv), dtype=torch.float32, device=q.device)
+    _cuda_contig(out, "out", torch.float32)
+    if lse is None and want_lse:
+        lse = torch.empty((nreq, H), dtype=torch.float32, device=q.device)
+    ws_bytes = 0
+    if split:
+        need = sparse_workspace_bytes(nreq)
+        if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    else:
+        workspace = None
+    code = lib().tts_sparse_attn_decode(
+        _ptr(q), nreq, H, dqk, int(dv), _ptr(kv_cache), pages, page_size, _ptr(page_tables),
+        page_tables.shape[1], _ptr(kv_lens), _ptr(idx), idx.shape[1], float(scale), _ptr(out),
+        _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(q.device))
+    _check(code, "tts_sparse_attn_decode")
+    return out, lse
+
+
+def paged_kv_write(kv_cache, page_tables, kv_new, positions, req_ids=None, status=None):
+    """Write rows into the paged KV cache (tts_paged_kv_write): token t's row kv_new[t]
+    goes to its request's page at logical position positions[t]. In place; returns
+    kv_cache."""
+    _cuda_contig(kv_cache, "kv_cache", torch.bfloat16)
+    _cuda_contig(page_tables, "page_tables", torch.int32)
+    _cuda_contig(kv_new, "kv_new", torch.bfloat16)
+    _cuda_contig(positions, "positions", torch.int32)
+    if req_ids is not None:
+        _cuda_contig(req_ids, "req_ids", torch.int32)
+    _need(kv_cache.dim() == 3 and kv_new.dim() == 2 and page_tables.dim() == 2, "ranks")
+    pages, page_size, dim = kv_cache.shape
+    ntok = kv_new.shape[0]
+    _need(kv_new.shape[1] == dim and positions.numel() == ntok and
+          (req_ids is None or req_ids.numel() == ntok), "shapes")
+    code = lib().tts_paged_kv_write(_ptr(kv_new), ntok, dim, _ptr(req_ids), _ptr(positions),
+                                    _ptr(page_tables), page_tables.shape[1],
+                                    page_tables.shape[0], _ptr(kv_cache), pages, page_size,
+                                    _ptr(status), _stream(kv_new.device))
+    _check(code, "tts_paged_kv_write")
+    return kv_cache
 
 
 def sparse_workspace_bytes(nq) -> int:

@@ -257,4 +257,70 @@ tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, i
   return from_cuda(e);
 }
 
+tts_status tts_sparse_attn_decode(const void* q, int32_t nreq, int32_t num_heads, int32_t dqk,
+                                  int32_t dv, const void* kv_cache, int32_t num_pages,
+                                  int32_t page_size, const int32_t* page_tables,
+                                  int32_t max_pages, const int32_t* kv_lens, const int32_t* idx,
+                                  int32_t topk, float scale, float* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                  void* stream) {
+  if (q == nullptr || kv_cache == nullptr || page_tables == nullptr || kv_lens == nullptr ||
+      idx == nullptr || out == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (workspace != nullptr && !aligned16(workspace)) return TTS_ERR_INVALID_ARG;
+  if (nreq < 0 || num_heads < 1 || dqk < 1 || dv < 1 || dv > dqk || num_pages < 1 ||
+      page_size < 1 || max_pages < 1 || topk < 1)
+    return TTS_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return TTS_ERR_INVALID_ARG;
+  if ((int64_t)num_pages * page_size > 0x7FFFFF00LL ||
+      (int64_t)max_pages * page_size > 0x7FFFFF00LL)
+    return TTS_ERR_UNSUPPORTED;
+  if (num_heads != 128 || dqk != 576 || dv != 512 || topk > 2048) return TTS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return TTS_ERR_INVALID_ARG;
+  if (nreq == 0) return TTS_OK;
+  SparseArgs a;
+  a.q = q;
+  a.kv_cache = kv_cache;
+  a.page_table = page_tables;
+  a.kv_lens = kv_lens;
+  a.pt_stride = max_pages;
+  a.idx = idx;
+  a.nq = nreq;
+  a.heads = num_heads;
+  a.dqk = dqk;
+  a.dv = dv;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.num_logical_pages = max_pages;
+  a.kv_len = 0;
+  a.topk = topk;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace == nullptr ? 0 : workspace_bytes;
+  a.dev_status = dev_status;
+  int drv = 0;
+  cudaError_t e = launch_sparse_attn(a, &drv, static_cast<cudaStream_t>(stream));
+  if (drv != 0) return TTS_ERR_CUDA;
+  return from_cuda(e);
+}
+
+tts_status tts_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
+                              const int32_t* req_ids, const int32_t* positions,
+                              const int32_t* page_tables, int32_t max_pages, int32_t nreq,
+                              void* kv_cache, int32_t num_pages, int32_t page_size,
+                              uint32_t* dev_status, void* stream) {
+  if (kv_new == nullptr || positions == nullptr || page_tables == nullptr || kv_cache == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (ntok < 0 || dim < 8 || dim % 8 != 0 || max_pages < 1 || nreq < 1 || num_pages < 1 ||
+      page_size < 1)
+    return TTS_ERR_INVALID_ARG;
+  if (!aligned16(kv_new) || !aligned16(kv_cache)) return TTS_ERR_INVALID_ARG;
+  if (ntok == 0) return TTS_OK;
+  return from_cuda(launch_paged_kv_write(kv_new, ntok, dim, req_ids, positions, page_tables,
+                                         max_pages, nreq, kv_cache, num_pages, page_size,
+                                         dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -18,6 +18,13 @@ cudaError_t launch_topk_long(const float* logits, int64_t row_stride, int32_t ro
                              int32_t* idx, void* workspace, uint32_t* dev_status,
                              cudaStream_t stream);
 
+// ---- paged KV cache write
+cudaError_t launch_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
+                                  const int32_t* req_ids, const int32_t* positions,
+                                  const int32_t* page_tables, int32_t max_pages, int32_t nreq,
+                                  void* kv_cache, int32_t num_pages, int32_t page_size,
+                                  uint32_t* dev_status, cudaStream_t stream);
+
 // ---- dense attention
 struct AttnArgs {
   const void* q;  // bf16
@@ -42,6 +49,8 @@ struct SparseArgs {
   const void* q;         // bf16 [nq, H, dqk]
   const void* kv_cache;  // bf16 [pages, page_size, dqk]
   const int32_t* page_table;
+  const int32_t* kv_lens = nullptr;  // decode: per-query lengths (else kv_len for all)
+  int pt_stride = 0;                 // decode: page-table row stride (else one shared table)
   const int32_t* idx;
   int nq, heads, dqk, dv, num_pages, page_size, num_logical_pages, kv_len, topk;
   float scale;

@@ -62,7 +62,9 @@ static_assert(kCountCap + kMaxTopk <= kScratchInts, "counts and the sorted list 
 struct SparseParams {
   const uint16_t* q;  // bf16 bits [nq, 128, 576]
   const uint16_t* kv;  // bf16 bits [pages * page_size, 576]
-  const int32_t* page_table;
+  const int32_t* page_table;  // row n of the tables starts at page_table + n * pt_stride
+  const int32_t* kv_lens;     // per query (decode), or nullptr: kv_len for every query
+  int pt_stride;              // 0: one table shared by all queries
   const int32_t* idx;
   float* out;
   float* lse;
@@ -164,9 +166,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Scratch in the (still unused) K stages: counts [kv_len] (counting sort only), a copy
   // of the page table when it fits, then the sorted list.
   const int32_t* idx_row = p.idx + (int64_t)n * p.topk;
-  const bool by_count = p.kv_len <= kCountCap;
+  const int32_t* const ptab = p.page_table + (int64_t)n * p.pt_stride;
+  int kv_len = p.kv_len;
+  if (p.kv_lens != nullptr) {
+    kv_len = p.kv_lens[n];
+    if (kv_len < 0) {  // every entry of this query is then out of range
+      if (tid == 0 && p.dev_status != nullptr) atomicOr(p.dev_status, kDevIndexRange);
+      kv_len = 0;
+    }
+  }
+  const bool by_count = kv_len <= kCountCap;
   const int n_scan = by_count ? p.topk : p.sort_n;
-  const int n_counts = by_count ? p.kv_len : 0;
+  const int n_counts = by_count ? kv_len : 0;
   const int nlp = p.num_logical_pages;
   const bool pt_cached = n_counts + nlp + n_scan <= kScratchInts;
   int32_t* counts = reinterpret_cast<int32_t*>(smem + kQhiBytes);
@@ -182,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   for (int v = tid; v < n_counts; v += kThreads) counts[v] = 0;
   if (pt_cached)
-    for (int g = tid; g < nlp; g += kThreads) pt[g] = p.page_table[g];
+    for (int g = tid; g < nlp; g += kThreads) pt[g] = ptab[g];
   __syncthreads();
-  auto page_of = [&](int g) -> int32_t { return pt_cached ? pt[g] : p.page_table[g]; };
+  auto page_of = [&](int g) -> int32_t { return pt_cached ? pt[g] : ptab[g]; };
   // logical position -> (logical page, offset); shifts for power-of-two page sizes
   auto lpage = [&](int v) { return p.page_shift >= 0 ? v >> p.page_shift : v / p.page_size; };
   auto row_of = [&](int v) -> int32_t {
@@ -199,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t i = iv[u];
     int key = 0x7FFFFFFF;
     if (i != -1 && j < p.topk) {
-      const bool in = i >= 0 && i < p.kv_len && lpage(i) < nlp;
+      const bool in = i >= 0 && i < kv_len && lpage(i) < nlp;
       const int32_t pg = in ? page_of(lpage(i)) : -1;
       if (pg >= 0 && pg < p.num_pages) {
         key = i;
@@ -219,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (by_count) {
     // Counting sort: thread t owns a contiguous range of positions; an exclusive scan
     // of the per-range totals gives where each range's entries start.
-    const int per = (p.kv_len + kThreads - 1) / kThreads;
-    const int v0 = tid * per, v1 = min(p.kv_len, v0 + per);
+    const int per = (kv_len + kThreads - 1) / kThreads;
+    const int v0 = tid * per, v1 = min(kv_len, v0 + per);
     int tot = 0;
     for (int v = v0; v < v1; ++v) tot += counts[v];
     int incl = tot;
@@ -716,6 +727,8 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
   p.q = static_cast<const uint16_t*>(a.q);
   p.kv = static_cast<const uint16_t*>(a.kv_cache);
   p.page_table = a.page_table;
+  p.kv_lens = a.kv_lens;
+  p.pt_stride = a.pt_stride;
   p.idx = a.idx;
   p.out = a.out;
   p.lse = a.lse;

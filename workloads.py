@@ -27,7 +27,8 @@ from dataclasses import dataclass, field
 
 import torch
 
-SEEDS = {"tiny": 0, "vision": 1, "varlen": 2, "topk": 3, "sparse": 4, "topk_long": 5}
+SEEDS = {"tiny": 0, "vision": 1, "varlen": 2, "topk": 3, "sparse": 4, "topk_long": 5,
+         "decode": 6}
 PERM_SEEDS = tuple(range(100, 108))
 
 
@@ -190,6 +191,55 @@ def sparse_inputs(nq=323, heads=128, dqk=576, dv=512, kv_len=2590, page_size=64,
         take = min(topk, win)
         idx[n, :take] = torch.randperm(win, generator=g)[:take].to(torch.int32)
     return SparseInputs(q, kv, page_table, idx, kv_len, dv, 1.0 / math.sqrt(dqk))
+
+
+@dataclass
+class DecodeInputs:
+    q: torch.Tensor            # bf16 [nreq, H, dqk]: each request's one new query
+    kv_cache: torch.Tensor     # bf16 [pages, page_size, dqk], a pool shared by the requests
+    page_tables: torch.Tensor  # int32 [nreq, max_pages]; -1 past a request's pages
+    kv_lens: torch.Tensor      # int32 [nreq]
+    idx: torch.Tensor          # int32 [nreq, topk] logical positions, -1 = empty slot
+    kv_new: torch.Tensor       # bf16 [nreq, dqk]: each request's next KV row
+    dv: int
+    scale: float
+
+    def gathered_bytes(self) -> int:
+        valid = int((self.idx >= 0).sum().item())
+        return valid * self.kv_cache.shape[2] * 2
+
+    def flops(self) -> float:
+        valid = int((self.idx >= 0).sum().item())
+        H, dqk = self.q.shape[1], self.q.shape[2]
+        return 2.0 * H * valid * (dqk + self.dv)
+
+
+def sparse_decode_inputs(kv_lens=(2590,) * 8, heads=128, dqk=576, dv=512, page_size=64,
+                         topk=2048, seed=None, spare_pages=3) -> DecodeInputs:
+    """Decode step of several requests: request n has kv_lens[n] tokens in its own pages,
+    drawn shuffled from one pool (plus room for one more token), and one query whose
+    top-k index list is a random subset of its positions (all of them when shorter)."""
+    g = _gen(SEEDS["decode"] if seed is None else seed)
+    nreq = len(kv_lens)
+    need = [(int(L) + 1 + page_size - 1) // page_size for L in kv_lens]  # + the next token
+    max_pages = max(need)
+    pool = sum(need) + spare_pages
+    order = torch.randperm(pool, generator=g).to(torch.int32)
+    page_tables = torch.full((nreq, max_pages), -1, dtype=torch.int32)
+    at = 0
+    for n, c in enumerate(need):
+        page_tables[n, :c] = order[at:at + c]
+        at += c
+    q = torch.randn(nreq, heads, dqk, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    kv = torch.randn(pool, page_size, dqk, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    idx = torch.full((nreq, topk), -1, dtype=torch.int32)
+    for n, L in enumerate(kv_lens):
+        take = min(topk, int(L))
+        if take > 0:
+            idx[n, :take] = torch.randperm(int(L), generator=g)[:take].to(torch.int32)
+    kv_new = torch.randn(nreq, dqk, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return DecodeInputs(q, kv, page_tables, torch.tensor(kv_lens, dtype=torch.int32), idx,
+                        kv_new, dv, 1.0 / math.sqrt(dqk))
 
 
 def permute_rows(idx: torch.Tensor, seed: int) -> torch.Tensor:
