@@ -17,6 +17,11 @@ arrays. Each function cites the passage of the pages it follows in that file:
   ("推理引擎的蝴蝶效应", 实验方法和结果; "AMD MI250部署", section 4.2).
 * ``sparse_paged`` -- gather through a page table, canonical ascending index
   order, then attention ("推理引擎的蝴蝶效应", 实验方法和结果 / 进一步探索).
+* ``qkv_rope`` / ``rope_cache`` -- the vision encoder's QKV projection followed by
+  rotary position embedding of q and k ("DeepSeek V4.1 上 4×RTX 3090", 坑 1) and the
+  position-indexed cos/sin cache ("从 SGLang Kernel源码到 GPU Trace", section 3.3);
+  the RoPE variant is not on the pages: one-dimensional, rotate-half pairs
+  (j, j + d/2), angle pos * base^(-2j/d), base 10000 unless given.
 * ``round_bf16`` -- round-to-nearest-even of fp32 values to the bf16 grid, the
   rounding the CUDA path applies to fp32 inputs at its boundary.
 
@@ -73,6 +78,10 @@ def _load():
             lib.oracle_sparse_paged.argtypes = [P, i64, i32, i32, i32, P, i64, i32, P, i64, i64,
                                                 P, i32, dbl, P, P]
             lib.oracle_sparse_paged.restype = ctypes.c_int64
+            lib.oracle_qkv_rope.argtypes = [P, i64, i32, P, P, i32, i32, P, dbl, P, P, P]
+            lib.oracle_qkv_rope.restype = None
+            lib.oracle_rope_cache.argtypes = [i32, i32, dbl, P]
+            lib.oracle_rope_cache.restype = None
             _lib = lib
     return _lib
 
@@ -155,3 +164,27 @@ def sparse_paged(q, kv_cache, page_table, idx, kv_len: int, dv: int, scale: floa
                                       pt.size, int(kv_len), _p(ix), topk_, float(scale),
                                       _p(out), _p(lse))
     return out, lse, int(bad)
+
+
+def qkv_rope(x, w, bias, positions, heads: int, d: int, base: float = 10000.0):
+    """QKV projection + RoPE. x [n, hidden], w [3*heads*d, hidden], bias [3*heads*d] or
+    None, positions [n]. Returns (q, k, v) float64 [n, heads, d]."""
+    x, w = _f32(x), _f32(w)
+    n, hidden = x.shape
+    assert w.shape == (3 * heads * d, hidden) and d % 2 == 0
+    b = None if bias is None else _f32(bias)
+    pos = _i32(positions)
+    assert pos.shape == (n,)
+    q = np.empty((n, heads, d), np.float64)
+    k = np.empty_like(q)
+    v = np.empty_like(q)
+    _load().oracle_qkv_rope(_p(x), n, hidden, _p(w), None if b is None else _p(b), heads, d,
+                            _p(pos), float(base), _p(q), _p(k), _p(v))
+    return q, k, v
+
+
+def rope_cache(max_pos: int, rot_dim: int, base: float = 10000.0):
+    """float64 [max_pos, rot_dim/2, 2]: (cos, sin) of pos * base^(-2j/rot_dim)."""
+    out = np.empty((max_pos, rot_dim // 2, 2), np.float64)
+    _load().oracle_rope_cache(int(max_pos), int(rot_dim), float(base), _p(out))
+    return out

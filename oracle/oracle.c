@@ -276,3 +276,60 @@ int64_t oracle_sparse_paged(const float* q, int64_t nq, int H, int dqk, int dv,
   }
   return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* O4. Vision-encoder QKV projection + RoPE ("DeepSeek V4.1 上 4×RTX 3090",   */
+/* 坑 1: the qkv + RoPE step checked block by block against a CPU reference; */
+/* the position-indexed cos/sin cache of "从 SGLang Kernel源码到 GPU Trace",  */
+/* section 3.3). The pages leave the RoPE variant open; the reading taken:   */
+/* one-dimensional rotary embedding of every q and k head, rotate-half pairs */
+/* (j, j + d/2), angle pos * base^(-2j/d).                                   */
+/*                                                                           */
+/* x    [n, hidden]; w [3 * heads * d, hidden] (rows: q heads, k heads, v    */
+/*      heads); bias [3 * heads * d] or NULL; pos [n].                        */
+/* q, k, v [n, heads, d] (double). Plain loops: y = w x + bias, then each q  */
+/* and k head rotated pair by pair; v as projected.                          */
+/* ------------------------------------------------------------------------ */
+void oracle_qkv_rope(const float* x, int64_t n, int hidden, const float* w, const float* bias,
+                     int heads, int d, const int32_t* pos, double base, double* q, double* k,
+                     double* v) {
+  const int64_t cols = 3LL * heads * d;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t t = 0; t < n; ++t) {
+    double* y = (double*)malloc(sizeof(double) * (size_t)cols);
+    for (int64_t c = 0; c < cols; ++c) {
+      double s = bias ? (double)bias[c] : 0.0;
+      for (int i = 0; i < hidden; ++i) s += (double)w[c * hidden + i] * (double)x[t * hidden + i];
+      y[c] = s;
+    }
+    for (int part = 0; part < 3; ++part) {
+      double* dst = part == 0 ? q : (part == 1 ? k : v);
+      for (int h = 0; h < heads; ++h) {
+        const double* src = y + ((int64_t)part * heads + h) * d;
+        double* o = dst + (t * heads + h) * (int64_t)d;
+        if (part == 2) {
+          for (int i = 0; i < d; ++i) o[i] = src[i];
+          continue;
+        }
+        for (int j = 0; j < d / 2; ++j) {
+          const double ang = (double)pos[t] * pow(base, -2.0 * j / d);
+          const double c = cos(ang), s = sin(ang);
+          const double a = src[j], b = src[j + d / 2];
+          o[j] = a * c - b * s;
+          o[j + d / 2] = a * s + b * c;
+        }
+      }
+    }
+    free(y);
+  }
+}
+
+/* The cos/sin cache: out[p, j] = (cos, sin)(p * base^(-2j/rot_dim)), p < max_pos. */
+void oracle_rope_cache(int max_pos, int rot_dim, double base, double* out) {
+  for (int p = 0; p < max_pos; ++p)
+    for (int j = 0; j < rot_dim / 2; ++j) {
+      const double ang = (double)p * pow(base, -2.0 * j / rot_dim);
+      out[((int64_t)p * (rot_dim / 2) + j) * 2] = cos(ang);
+      out[((int64_t)p * (rot_dim / 2) + j) * 2 + 1] = sin(ang);
+    }
+}

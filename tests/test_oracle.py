@@ -380,3 +380,74 @@ def test_sparse_skips_and_counts_bad_entries():
     o2, l2, b2 = _sparse(inp, badi)
     assert b1 == 0 and b2 == 3
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---- QKV projection + RoPE ------------------------------------------------------------
+
+def _proj(x, w, b):
+    """The projection alone, by numpy's float64 matmul (a routine the oracle does not call)."""
+    y = x.astype(np.float64) @ w.astype(np.float64).T
+    return y if b is None else y + b.astype(np.float64)
+
+
+def test_qkv_rope_worked_example_and_bias():
+    # d = 4, base 10000: pair (0, 2) turns by pos * 1, pair (1, 3) by pos * 0.01
+    x = np.array([[1, 0, 0, 0], [0, 1, 0, 0], [1, 0, 0, 0]], np.float32)
+    w = np.vstack([np.eye(4)] * 3).astype(np.float32)   # q = k = v = x
+    q, k, v = oracle.qkv_rope(x, w, None, [1, 1, 3], heads=1, d=4)
+    c1, s1, c2, s2 = math.cos(1.0), math.sin(1.0), math.cos(0.01), math.sin(0.01)
+    np.testing.assert_allclose(q[0, 0], [c1, 0, s1, 0], atol=1e-15)
+    np.testing.assert_allclose(q[1, 0], [0, c2, 0, s2], atol=1e-15)
+    np.testing.assert_allclose(q[2, 0], [math.cos(3.0), 0, math.sin(3.0), 0], atol=1e-15)
+    np.testing.assert_array_equal(k, q)
+    np.testing.assert_array_equal(v[:, 0], x)            # v is not rotated
+    # the bias is added before the rotation: bias e_2 on q turns (1, 0, 1, 0) at pos 1
+    b = np.zeros(12, np.float32)
+    b[2] = 1.0
+    qb, kb, _ = oracle.qkv_rope(x[:1], w, b, [1], heads=1, d=4)
+    np.testing.assert_allclose(qb[0, 0], [c1 - s1, 0, s1 + c1, 0], atol=1e-15)
+    np.testing.assert_allclose(kb[0, 0], [c1, 0, s1, 0], atol=1e-15)
+
+
+def test_qkv_rope_position_zero_is_the_projection():
+    rng = np.random.default_rng(30)
+    heads, d, hidden, n = 3, 80, 96, 17
+    x = rng.standard_normal((n, hidden)).astype(np.float32)
+    w = rng.standard_normal((3 * heads * d, hidden)).astype(np.float32)
+    b = rng.standard_normal(3 * heads * d).astype(np.float32)
+    q, k, v = oracle.qkv_rope(x, w, b, np.zeros(n), heads, d)
+    y = _proj(x, w, b).reshape(n, 3, heads, d)
+    for got, part in ((q, 0), (k, 1), (v, 2)):
+        np.testing.assert_allclose(got, y[:, part], rtol=1e-12, atol=1e-10)
+
+
+def test_qkv_rope_keeps_pair_norms_and_relative_positions():
+    rng = np.random.default_rng(31)
+    heads, d, hidden, n = 2, 80, 64, 6
+    x = rng.standard_normal((n, hidden)).astype(np.float32)
+    w = rng.standard_normal((3 * heads * d, hidden)).astype(np.float32)
+    pos = rng.integers(0, 8547, n)
+    q, k, _ = oracle.qkv_rope(x, w, None, pos, heads, d)
+    y = _proj(x, w, None).reshape(n, 3, heads, d)
+    h = d // 2
+    for got, part in ((q, 0), (k, 1)):
+        norm_got = np.hypot(got[..., :h], got[..., h:])
+        norm_raw = np.hypot(y[:, part, :, :h], y[:, part, :, h:])
+        np.testing.assert_allclose(norm_got, norm_raw, rtol=1e-12)
+    # q(m) . k(n) depends on m - n only: shift every position by the same amount
+    q2, k2, _ = oracle.qkv_rope(x, w, None, pos + 1234, heads, d)
+    dots = np.einsum("ihd,jhd->hij", q, k)
+    dots2 = np.einsum("ihd,jhd->hij", q2, k2)
+    np.testing.assert_allclose(dots2, dots, rtol=1e-9, atol=1e-8)
+    # ... but not on the positions alone: a shift of only the keys changes it
+    _, k3, _ = oracle.qkv_rope(x, w, None, pos + 7, heads, d)
+    assert np.abs(np.einsum("ihd,jhd->hij", q, k3) - dots).max() > 1e-3
+
+
+def test_rope_cache_rows_are_powers_of_the_first():
+    c = oracle.rope_cache(300, 80)
+    z = c[..., 0] + 1j * c[..., 1]                      # [pos, 40] unit complex numbers
+    np.testing.assert_allclose(z[0], np.ones(40), atol=0)
+    p = np.arange(300)[:, None]
+    np.testing.assert_allclose(z, np.power(z[1][None, :], p), atol=1e-11)
+    np.testing.assert_allclose(np.abs(z), 1.0, atol=1e-15)
