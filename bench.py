@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNELS = {"vision": "attn_fwd_kernel<80>", "varlen": "attn_fwd_kernel<128>",
            "topk": "topk_select_kernel", "sparse": "sparse_attn_kernel"}
 KERNEL_SOURCES = {"vision": "attn_fwd.cu", "varlen": "attn_fwd.cu", "topk": "topk.cu",
-                  "sparse": "sparse_attn.cu"}
+                  "sparse": "sparse_attn.cu", "vision_qkv_rope": "qkv_rope.cu"}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -447,6 +447,54 @@ def decode_protocol(step, dev, peaks):
             "protocol": "CUDA graph of 20 calls, two alternating index sets (302 MB gathered)"}
 
 
+def qkv_rope_protocol(step, dev, peaks, flush):
+    """Vision QKV projection + RoPE outside the step (the projection in front of the
+    vision attention): 8547 tokens, hidden 1280, 16 heads of 80, positions 0..8546,
+    cos/sin table of 32768 positions (built once, outside the timing). Each of 20
+    calls is timed alone with CUDA events on its stream after a 256 MB L2 flush; the
+    median is reported. The q / k / v of every call are checked against the first."""
+    t = step.tts
+    inp = W.vision_qkv_inputs()
+    x, w = inp.x.to(dev), inp.w.to(dev)
+    b, pos = inp.bias.to(dev), inp.positions.to(dev)
+    cs = t.rope_cache(inp.max_pos, inp.d, inp.base, device=dev)
+    n, hidden = inp.x.shape
+    H, d = inp.heads, inp.d
+    outs = [torch.empty((n, H, d), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    ref = None
+    s = torch.cuda.Stream(dev)
+    times = []
+    with torch.cuda.stream(s):
+        for it in range(24):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            t.qkv_rope(x, w, b, pos, cs, H, q=outs[0], k=outs[1], v=outs[2], status=step.status)
+            e1.record(s)
+            e1.synchronize()
+            if it >= 4:
+                times.append(e0.elapsed_time(e1) * 1e3)
+            if ref is None:
+                ref = [o.clone() for o in outs]
+    for o, r in zip(outs, ref):
+        assert torch.equal(o, r), "qkv_rope: calls disagree"
+    us = float(np.median(times))
+    flops = inp.flops()
+    tf = flops / (us * 1e-6) / 1e12
+    nbytes = (n * hidden + inp.w.numel()) * 2 + 3 * n * H * d * 2 + b.numel() * 4 + n * 4
+    del x, w, outs, ref, cs
+    return {"workload": f"{n} tokens x hidden {hidden} -> q/k/v {H} heads x {d} "
+                        f"(RoPE on q, k; table of {inp.max_pos} positions)",
+            "kernel": "qkv_rope_kernel<80>", "us_per_call": us, "flops": flops,
+            "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
+            "peak_source": "bf16_tflops (a call timed alone)",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                         "traffic": profiled_traffic("vision_qkv_rope")},
+            "bytes": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9,
+            "protocol": "median of 20 single calls, CUDA events, L2 flushed before each"}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(n_rows: int = 192, n_queries: int = 8):
     """Time the float64 oracle on bounded samples of each part.
@@ -637,6 +685,9 @@ def run_gpu(args, rank, world, local):
     if "topk" in parts and rank == 0:
         comp["topk"].update(topk_protocol(step, dev, peaks))
         comp["topk_long"] = topk_long_protocol(step, dev, peaks)
+    if "vision" in parts and rank == 0:
+        comp["vision_qkv_rope"] = qkv_rope_protocol(step, dev, peaks, flush)
+        tts.check_status(step.status, "bench qkv_rope protocol")
     if "sparse" in parts and rank == 0:
         comp["sparse_decode"] = decode_protocol(step, dev, peaks)
         tts.check_status(step.status, "bench decode protocol")

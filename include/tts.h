@@ -254,6 +254,61 @@ tts_status tts_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
 size_t tts_sparse_workspace_bytes(int32_t nq);
 
 /*
+ * cos/sin table of rotary position embedding, built once and read by tts_qkv_rope.
+ *
+ * The position-indexed table of "从 SGLang Kernel源码到 GPU Trace" (section 3.3: cos
+ * and sin of every position up to the longest sequence, computed ahead of the
+ * prefill instead of inside it). For position p < max_pos and pair j < rot_dim / 2:
+ *   cos_sin[(p * rot_dim/2 + j) * 2 + 0] = cos(p * base^(-2j / rot_dim))
+ *   cos_sin[(p * rot_dim/2 + j) * 2 + 1] = sin(p * base^(-2j / rot_dim))
+ * The angle and its cosine / sine are evaluated in double precision and rounded to
+ * fp32 once.
+ *
+ * cos_sin  device fp32 [max_pos, rot_dim / 2, 2], 16-byte aligned, written.
+ * max_pos >= 1, rot_dim even and >= 2, base > 1 and finite; otherwise
+ * TTS_ERR_INVALID_ARG and nothing is enqueued.
+ */
+tts_status tts_rope_cache(int32_t max_pos, int32_t rot_dim, float base, float* cos_sin,
+                          void* stream);
+
+/*
+ * Vision-encoder QKV projection fused with rotary position embedding.
+ *
+ * The qkv + RoPE step of the vision encoder in "DeepSeek V4.1 上 4×RTX 3090：视觉链路
+ * 的两个坑和修复" (坑 1, checked block by block against a CPU reference), reading its
+ * cos/sin from the table of tts_rope_cache ("从 SGLang Kernel源码到 GPU Trace",
+ * section 3.3). For token t, with y = W x[t] + bias (y has 3 * H * d entries: the H
+ * q heads, then the H k heads, then the H v heads, d each):
+ *   q[t,h,j]       = y_q[j] c - y_q[j + d/2] s      for j < d/2,
+ *   q[t,h,j + d/2] = y_q[j] s + y_q[j + d/2] c      (c, s) = cos_sin[positions[t], j]
+ * and the same for k; v[t,h,:] = y_v. The pages do not fix the RoPE variant; this
+ * is one-dimensional rotate-half RoPE on the full head (pairs j, j + d/2).
+ * The products run on the tensor cores with bf16 operands and an fp32 accumulator;
+ * bias and rotation are applied in fp32; results are rounded to bf16 (nearest even).
+ *
+ * x          device bf16 [n, hidden], row-major
+ * w          device bf16 [3 * num_heads * head_dim, hidden], row-major (the weight
+ *            of a linear layer: one row per output feature)
+ * bias       device fp32 [3 * num_heads * head_dim], or NULL for none
+ * positions  device int32 [n]; an entry outside [0, max_pos) is skipped: that token's
+ *            q and k are written as zeros and TTS_DEV_INDEX_RANGE is set
+ * cos_sin    device fp32 [max_pos, head_dim / 2, 2] as written by tts_rope_cache
+ *            (rot_dim = head_dim)
+ * q, k, v    device bf16 [n, num_heads, head_dim], written
+ * head_dim in {64, 80, 128}; 3 * num_heads must be a multiple of the heads per output
+ * tile (3 for head_dim 80, 4 for 64, 2 for 128): otherwise TTS_ERR_UNSUPPORTED.
+ * hidden >= 8 and a multiple of 8; x, w, q, k, v, bias and cos_sin 16-byte aligned;
+ * n <= 2^31 - 1; otherwise TTS_ERR_INVALID_ARG. n = 0 enqueues nothing and accepts
+ * null data pointers (after the size checks above). Nothing is
+ * allocated; every output element is written by exactly one thread, so the result is
+ * bitwise reproducible.
+ */
+tts_status tts_qkv_rope(const void* x, int64_t n, int32_t hidden, const void* w,
+                        const float* bias, const int32_t* positions, const float* cos_sin,
+                        int32_t max_pos, int32_t num_heads, int32_t head_dim, void* q, void* k,
+                        void* v, uint32_t* dev_status, void* stream);
+
+/*
  * Diagnostics (no counterpart in the pages): launches one thread that waits on a
  * barrier phase nothing completes. The wait is bounded like every wait in the library:
  * after about one second it ORs TTS_DEV_TIMEOUT into *dev_status (device pointer,

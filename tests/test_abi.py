@@ -181,3 +181,45 @@ def test_product_has_no_cpu_fallback():
         if fn.endswith(".py"):
             src = open(os.path.join(pkg, fn)).read()
             assert "import oracle" not in src and "from oracle" not in src, fn
+
+
+def test_qkv_rope_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    f = L.tts_qkv_rope
+    A = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced
+    ok = (A, 300, 1280, A, A, A, A, 32768, 16, 80, A, A, A, NUL, NUL)
+
+    def call(**kw):
+        names = ("x", "n", "hidden", "w", "bias", "pos", "cs", "max_pos", "heads", "d", "q",
+                 "k", "v", "st", "stream")
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return f(*[args[n] for n in names])
+
+    for name in ("x", "w", "pos", "cs", "q", "k", "v"):
+        assert call(**{name: NUL}) == tts.TTS_ERR_INVALID_ARG, name
+    assert call(n=-1) == tts.TTS_ERR_INVALID_ARG
+    assert call(hidden=1284) == tts.TTS_ERR_INVALID_ARG       # rows not 16-byte strided
+    assert call(hidden=0) == tts.TTS_ERR_INVALID_ARG
+    assert call(max_pos=0) == tts.TTS_ERR_INVALID_ARG
+    assert call(heads=0) == tts.TTS_ERR_INVALID_ARG
+    assert call(x=ctypes.c_void_p(0x10008)) == tts.TTS_ERR_INVALID_ARG  # misaligned
+    assert call(bias=ctypes.c_void_p(0x10004)) == tts.TTS_ERR_INVALID_ARG
+    assert call(d=96) == tts.TTS_ERR_UNSUPPORTED
+    assert call(d=128, heads=3) == tts.TTS_ERR_UNSUPPORTED    # 9 heads: not 2 per tile
+    assert call(d=64, heads=3) == tts.TTS_ERR_UNSUPPORTED     # 9 heads: not 4 per tile
+    assert call(n=0) == tts.TTS_OK                            # nothing to do
+    assert call(n=0, bias=NUL) == tts.TTS_OK
+
+
+def test_rope_cache_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    f = L.tts_rope_cache
+    A = ctypes.c_void_p(0x10000)
+    assert f(0, 80, 10000.0, A, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(10, 79, 10000.0, A, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(10, 0, 10000.0, A, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(10, 80, 1.0, A, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(10, 80, float("inf"), A, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(10, 80, 10000.0, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
+    assert f(10, 80, 10000.0, ctypes.c_void_p(0x10004), NUL) == tts.TTS_ERR_INVALID_ARG

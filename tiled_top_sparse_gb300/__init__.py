@@ -9,6 +9,9 @@ no fallback: if the library is missing or fails to load, calls raise.
     topk_select(logits, row_starts, row_lens, k, idx=None, status=None)
     sparse_attn_paged(q, kv_cache, page_table, idx, kv_len, scale, dv=512,
                       out=None, lse=None, status=None)
+    rope_cache(max_pos, rot_dim, base=10000.0, out=None, device=None)
+    qkv_rope(x, w, bias, positions, cos_sin, num_heads, q=None, k=None, v=None,
+             status=None)
 
 `status`, when given, is a 1-element int32 CUDA tensor the kernels OR their
 device-side flags into (see TTS_DEV_* in the header); `check_status(status)`
@@ -50,6 +53,8 @@ EXPORTED = (
     "tts_sparse_workspace_bytes",
     "tts_sparse_attn_decode",
     "tts_paged_kv_write",
+    "tts_rope_cache",
+    "tts_qkv_rope",
     "tts_attn_fwd_varlen_f32_noalloc",
     "tts_debug_wait_timeout",
 )
@@ -100,6 +105,10 @@ def lib() -> ctypes.CDLL:
     L.tts_paged_kv_write.restype = ctypes.c_int
     L.tts_sparse_workspace_bytes.argtypes = [i32]
     L.tts_sparse_workspace_bytes.restype = ctypes.c_size_t
+    L.tts_rope_cache.argtypes = [i32, i32, f32, P, P]
+    L.tts_rope_cache.restype = ctypes.c_int
+    L.tts_qkv_rope.argtypes = [P, i64, i32, P, P, P, P, i32, i32, i32, P, P, P, P, P]
+    L.tts_qkv_rope.restype = ctypes.c_int
     L.tts_attn_fwd_varlen_f32_noalloc.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, i32,
                                                   i32, i32, i32, f32, P, P, P, P]
     L.tts_attn_fwd_varlen_f32_noalloc.restype = ctypes.c_int
@@ -348,3 +357,53 @@ def sparse_attn_paged(q, kv_cache, page_table, idx, kv_len, scale, dv=512, out=N
         _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(q.device))
     _check(code, "tts_sparse_attn_paged")
     return out, lse
+
+
+def rope_cache(max_pos, rot_dim, base=10000.0, out=None, device=None):
+    """cos/sin table of rotary embedding (tts_rope_cache): fp32 [max_pos, rot_dim/2, 2]
+    holding (cos, sin) of p * base^(-2j/rot_dim)."""
+    if out is None:
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        out = torch.empty((int(max_pos), int(rot_dim) // 2, 2), dtype=torch.float32, device=dev)
+    _cuda_contig(out, "out", torch.float32)
+    _need(tuple(out.shape) == (int(max_pos), int(rot_dim) // 2, 2), "out shape")
+    code = lib().tts_rope_cache(int(max_pos), int(rot_dim), float(base), _ptr(out),
+                                _stream(out.device))
+    _check(code, "tts_rope_cache")
+    return out
+
+
+def qkv_rope(x, w, bias, positions, cos_sin, num_heads, q=None, k=None, v=None, status=None):
+    """Vision QKV projection + RoPE (tts_qkv_rope).
+
+    x bf16 [n, hidden], w bf16 [3*H*d, hidden], bias fp32 [3*H*d] or None, positions
+    int32 [n], cos_sin fp32 [max_pos, d/2, 2] (rope_cache with rot_dim = d). Returns
+    (q, k, v) bf16 [n, H, d]: q and k rotated, v as projected."""
+    _cuda_contig(x, "x", torch.bfloat16)
+    _cuda_contig(w, "w", torch.bfloat16)
+    _cuda_contig(positions, "positions", torch.int32)
+    _cuda_contig(cos_sin, "cos_sin", torch.float32)
+    _need(x.dim() == 2 and w.dim() == 2 and w.shape[1] == x.shape[1], "x [n, hidden], "
+          "w [3*H*d, hidden]")
+    n, hidden = x.shape
+    H = int(num_heads)
+    _need(w.shape[0] % (3 * H) == 0, "w rows must be 3 * num_heads * head_dim")
+    d = w.shape[0] // (3 * H)
+    _need(positions.numel() == n, "positions size")
+    _need(cos_sin.dim() == 3 and cos_sin.shape[1] == d // 2 and cos_sin.shape[2] == 2,
+          "cos_sin must be [max_pos, head_dim/2, 2]")
+    if bias is not None:
+        _cuda_contig(bias, "bias", torch.float32)
+        _need(bias.numel() == 3 * H * d, "bias size")
+    outs = []
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if t is None:
+            t = torch.empty((n, H, d), dtype=torch.bfloat16, device=x.device)
+        _cuda_contig(t, name, torch.bfloat16)
+        _need(tuple(t.shape) == (n, H, d), f"{name} shape")
+        outs.append(t)
+    code = lib().tts_qkv_rope(_ptr(x), n, hidden, _ptr(w), _ptr(bias), _ptr(positions),
+                              _ptr(cos_sin), cos_sin.shape[0], H, d, _ptr(outs[0]),
+                              _ptr(outs[1]), _ptr(outs[2]), _ptr(status), _stream(x.device))
+    _check(code, "tts_qkv_rope")
+    return tuple(outs)

@@ -323,4 +323,51 @@ tts_status tts_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
                                          dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+tts_status tts_rope_cache(int32_t max_pos, int32_t rot_dim, float base, float* cos_sin,
+                          void* stream) {
+  if (cos_sin == nullptr || !aligned16(cos_sin)) return TTS_ERR_INVALID_ARG;
+  if (max_pos < 1 || rot_dim < 2 || rot_dim % 2 != 0) return TTS_ERR_INVALID_ARG;
+  if (!(base > 1.f) || !std::isfinite(base)) return TTS_ERR_INVALID_ARG;
+  return from_cuda(launch_rope_cache(max_pos, rot_dim, static_cast<double>(base), cos_sin,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+tts_status tts_qkv_rope(const void* x, int64_t n, int32_t hidden, const void* w,
+                        const float* bias, const int32_t* positions, const float* cos_sin,
+                        int32_t max_pos, int32_t num_heads, int32_t head_dim, void* q, void* k,
+                        void* v, uint32_t* dev_status, void* stream) {
+  if (n < 0 || n > 0x7FFFFFFFLL || hidden < 8 || hidden % 8 != 0 || max_pos < 1 ||
+      num_heads < 1 || head_dim < 2)
+    return TTS_ERR_INVALID_ARG;
+  const int hpt = qkv_heads_per_tile(head_dim);
+  if (hpt == 0 || (3LL * num_heads) % hpt != 0) return TTS_ERR_UNSUPPORTED;
+  if ((int64_t)num_heads * head_dim > 0x7FFFFFFFLL / 3) return TTS_ERR_UNSUPPORTED;
+  if (n == 0) return TTS_OK;  // empty tensors may come with null data pointers
+  if (x == nullptr || w == nullptr || positions == nullptr || cos_sin == nullptr ||
+      q == nullptr || k == nullptr || v == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(cos_sin) || (bias != nullptr && !aligned16(bias)))
+    return TTS_ERR_INVALID_ARG;
+  QkvArgs a;
+  a.x = x;
+  a.w = w;
+  a.bias = bias;
+  a.positions = positions;
+  a.cos_sin = cos_sin;
+  a.n = n;
+  a.hidden = hidden;
+  a.heads = num_heads;
+  a.head_dim = head_dim;
+  a.max_pos = max_pos;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dev_status = dev_status;
+  int drv = 0;
+  cudaError_t e = launch_qkv_rope(a, &drv, static_cast<cudaStream_t>(stream));
+  if (drv != 0) return TTS_ERR_CUDA;
+  return from_cuda(e);
+}
+
 }  // extern "C"

@@ -65,6 +65,26 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
 // device with `sms` SMs (0: no split for this shape).
 size_t sparse_split_workspace_bytes(int nq, int sms);
 
+// ---- vision QKV projection + RoPE
+struct QkvArgs {
+  const void* x;  // bf16 [n, hidden]
+  const void* w;  // bf16 [3 * heads * head_dim, hidden]
+  const float* bias;
+  const int32_t* positions;
+  const float* cos_sin;  // [max_pos, head_dim / 2, 2]
+  int64_t n;
+  int hidden, heads, head_dim, max_pos;
+  void* q;
+  void* k;
+  void* v;
+  uint32_t* dev_status;
+};
+// Heads per output tile for head_dim (0: head_dim not built).
+int qkv_heads_per_tile(int head_dim);
+cudaError_t launch_qkv_rope(const QkvArgs& a, int* drv_err, cudaStream_t stream);
+cudaError_t launch_rope_cache(int max_pos, int rot_dim, double base, float* cos_sin,
+                              cudaStream_t stream);
+
 // ---- tensor maps (driver entry point fetched through the runtime)
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
                            void* base, const uint64_t* dims, const uint64_t* strides_bytes,

@@ -1,0 +1,427 @@
+// Vision-encoder QKV projection fused with rotary position embedding, and the
+// position-indexed cos/sin table it reads.
+//
+// What it computes ("DeepSeek V4.1 上 4×RTX 3090", 坑 1: the qkv + RoPE step of the
+// vision encoder; "从 SGLang Kernel源码到 GPU Trace", section 3.3: cos/sin of every
+// position precomputed once into a small cached table that the projection kernel
+// reads): y = x W^T + bias for every token, split into q, k and v heads; every q
+// and k head is turned pair by pair, pairs (j, j + d/2) by the angle
+// pos * base^(-2j/d); v is written as projected. The pages leave the RoPE variant
+// open; this one-dimensional rotate-half form is the reading taken.
+//
+// How: a persistent tcgen05 GEMM. Output tiles are 128 tokens x (whole heads:
+// 3 heads of 80, 4 of 64 or 2 of 128 columns), so a row's rotation partner is
+// always in the same thread's tile row and the rotation happens in the epilogue,
+// between TMEM and the store -- y never goes to global memory unrotated, so no
+// two threads ever write the same output element (the race of the vision
+// write-up has no place to happen).
+//   warp 0      TMA producer: x (128 x 64) and W (BN x 64) boxes, 128-byte
+//               swizzle, into a four-stage ring (three for d = 128)
+//   warp 1      TMEM allocator + MMA issuer: D[tmem] += x W^T, kind::f16, bf16
+//               operands, fp32 accumulator; two accumulators (columns 0 / 256)
+//               so the epilogue of one tile overlaps the next tile's MMAs
+//   warps 2..5  epilogue, one token row per thread (TMEM lane = warp % 4):
+//               + bias, rotation in fp32, bf16 rounding (nearest even), staged
+//               per head in shared memory and written by TMA stores (rows past
+//               the last token are clipped by the tensor map)
+// Tiles go to CTAs round-robin (tile t -> CTA t mod grid), n-tiles of one
+// token tile on neighbouring CTAs so its x box is read from L2.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tts {
+namespace {
+
+constexpr int kQkvThreads = 192;
+constexpr int kBM = 128;  // tokens per tile
+constexpr int kBK = 64;   // hidden columns per stage (one 128-byte swizzle row)
+
+template <int D>
+struct QkvCfg {
+  static constexpr int kHpt = (D == 80) ? 3 : 256 / D;  // heads per tile
+  static constexpr int kBN = kHpt * D;                  // 240 / 256 / 256
+  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr int kABytes = kBM * 128;
+  static constexpr int kBBytes = kBN * 128;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kOutBytes = 32 * D * 2;  // one head of one warp's 32 rows, bf16
+  static constexpr int kSmemBytes = kStages * kStageBytes + 4 * 2 * kOutBytes + 1024;
+  static_assert(kBN % 16 == 0 && kBN <= 256, "MMA N");
+  static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
+  static_assert(kSmemBytes + 256 <= 232448, "shared memory");
+};
+
+struct QkvMaps {
+  CUtensorMap x;       // {hidden, n} bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap w;       // {hidden, 3 H D} bf16, box {64, BN}, 128-byte swizzle
+  CUtensorMap out[3];  // q, k, v: {H D, n} bf16, box {D, 32}, no swizzle
+};
+
+struct QkvParams {
+  const float* bias;      // [3 H D] or null
+  const int32_t* pos;     // [n]
+  const float2* cos_sin;  // [max_pos, D/2] (cos, sin)
+  uint32_t* dev_status;
+  int n, heads, max_pos, tiles_n, n_tiles, k_steps;
+};
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+// Wait until at most one bulk group of this thread is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kQkvThreads, 1)
+    qkv_rope_kernel(const __grid_constant__ QkvMaps maps, const QkvParams p) {
+  using C = QkvCfg<D>;
+  constexpr int NS = C::kStages;
+  constexpr int H2 = D / 2;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_acc_full[2],
+      bar_acc_empty[2], bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  auto sA = [&](int st) { return s_base + st * C::kStageBytes; };
+  auto sB = [&](int st) { return s_base + st * C::kStageBytes + C::kABytes; };
+  uint8_t* out_base = smem + NS * C::kStageBytes;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_acc_full[i]), 1);
+      mbar_init(smem_u32(&bar_acc_empty[i]), 4);  // lane 0 of each epilogue warp
+    }
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&maps.x);
+      prefetch_tmap(&maps.w);
+      int g = 0;  // stages filled so far (ring position and phase)
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+        const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+        for (int ks = 0; ks < p.k_steps; ++ks, ++g) {
+          const int st = g % NS;
+          if (g >= NS && !mbar_wait(smem_u32(&bar_empty[st]), ((g / NS) - 1) & 1, abort_flag,
+                                    p.dev_status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bf = smem_u32(&bar_full[st]);
+          mbar_arrive_expect_tx(bf, C::kStageBytes);
+          tma_load_2d(sA(st), &maps.x, bf, ks * kBK, tm * kBM);
+          tma_load_2d(sB(st), &maps.w, bf, ks * kBK, tn * C::kBN);
+        }
+      }
+      if (!ok) {
+        // Best-effort drain: the latest armed phase of each stage is the only one
+        // that can still have copies in flight.
+        for (int j = g - 1; j >= 0 && j >= g - NS; --j)
+          mbar_wait(smem_u32(&bar_full[j % NS]), (j / NS) & 1, nullptr, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t e = elect_one();
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, C::kBN, 0, 0);
+    int g = 0, i = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++i) {
+      const int a = i & 1;
+      if (i >= 2 && !warp_wait(smem_u32(&bar_acc_empty[a]), ((i >> 1) - 1) & 1, abort_flag,
+                               p.dev_status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + a * 256;
+      for (int ks = 0; ks < p.k_steps; ++ks, ++g) {
+        const int st = g % NS;
+        if (!warp_wait(smem_u32(&bar_full[st]), (g / NS) & 1, abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = smem_desc(sA(st), 16, 1024, kSw128);
+        const uint64_t bd = smem_desc(sB(st), 16, 1024, kSw128);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)  // 32-byte steps inside the swizzle row
+          mma_ss_elect(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0, e);
+        mma_commit_elect(smem_u32(&bar_empty[st]), e);
+      }
+      if (!ok) break;
+      mma_commit_elect(smem_u32(&bar_acc_full[a]), e);
+    }
+    // Every MMA issued by this warp completes before TMEM is freed.
+    mma_commit_elect(smem_u32(&bar_drain), e);
+    mbar_wait(smem_u32(&bar_drain), 0, nullptr, p.dev_status);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;  // TMEM lane quarter = rows q4*32 .. q4*32+31 of the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    uint8_t* obuf[2] = {out_base + ((warp - 2) * 2) * C::kOutBytes,
+                        out_base + ((warp - 2) * 2 + 1) * C::kOutBytes};
+    int nstore = 0;  // heads staged so far by this warp (staging buffer = nstore & 1)
+    int i = 0;
+    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++i) {
+      const int a = i & 1;
+      if (!warp_wait(smem_u32(&bar_acc_full[a]), (i >> 1) & 1, abort_flag, p.dev_status)) break;
+      tc_fence_after();
+      const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+      const int row0 = tm * kBM + q4 * 32;  // this warp's first token
+      const int row = row0 + lane;
+      // A warp whose 32 rows all lie past the last token only frees the accumulator.
+      const bool live = row0 < p.n;
+      const int hh0 = tn * C::kHpt;  // first head column of the tile, in [0, 3H)
+      // Position of this thread's token; a position outside the table is reported,
+      // and that token's q and k are written as zeros.
+      int pos = 0;
+      bool pos_ok = true;
+      if (live && row < p.n && hh0 < 2 * p.heads) {
+        pos = p.pos[row];
+        pos_ok = pos >= 0 && pos < p.max_pos;
+        if (!pos_ok) {
+          if (p.dev_status) atomicOr(p.dev_status, kDevIndexRange);
+          pos = 0;
+        }
+      }
+      const float4* cs4 =
+          reinterpret_cast<const float4*>(p.cos_sin + static_cast<int64_t>(pos) * H2);
+      // d <= 80: the token's cos/sin row (d/2 pairs) is kept in registers for the tile.
+      constexpr bool kCsRegs = D <= 80;
+      float4 csr[kCsRegs ? H2 / 2 : 1];
+      if constexpr (kCsRegs) {
+        if (live && hh0 < 2 * p.heads) {
+#pragma unroll
+          for (int u = 0; u < H2 / 2; ++u) csr[u] = __ldg(cs4 + u);
+        }
+      }
+#pragma unroll 1
+      for (int hl = 0; hl < C::kHpt; ++hl) {
+        const int hh = hh0 + hl;
+        const int part = hh / p.heads, head = hh - part * p.heads;
+        const bool rot = part < 2;
+        const float* bias = p.bias ? p.bias + static_cast<int64_t>(hh) * D : nullptr;
+        const uint32_t tcol = lane_base + a * 256 + hl * D;
+        uint8_t* buf = obuf[nstore & 1];
+        // The store that last read this buffer (two stores ago) must be done reading.
+        if (live && lane == 0) bulk_wait_read_1();
+        __syncwarp();
+        uint8_t* myrow = buf + lane * (D * 2);
+        if (live) {
+#pragma unroll
+          for (int j0 = 0; j0 < H2; j0 += 8) {
+            uint32_t lo[8], hi[8];
+            tmem_ld8(tcol + j0, lo);
+            tmem_ld8(tcol + H2 + j0, hi);
+            tmem_ld_wait();
+            float ylo[8], yhi[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              ylo[u] = __uint_as_float(lo[u]);
+              yhi[u] = __uint_as_float(hi[u]);
+            }
+            if (bias != nullptr) {
+              const float4* b4 = reinterpret_cast<const float4*>(bias);
+              const float4 b0 = __ldg(b4 + j0 / 4), b1 = __ldg(b4 + j0 / 4 + 1);
+              const float4 c0 = __ldg(b4 + (H2 + j0) / 4), c1 = __ldg(b4 + (H2 + j0) / 4 + 1);
+              const float bl[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+              const float bh[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                ylo[u] += bl[u];
+                yhi[u] += bh[u];
+              }
+            }
+            if (rot) {
+              float cs[16];  // (cos, sin) of pairs j0 .. j0+7
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float4 v = kCsRegs ? csr[(j0 / 2 + u) % (kCsRegs ? H2 / 2 : 1)]
+                                         : __ldg(cs4 + j0 / 2 + u);
+                cs[4 * u] = v.x;
+                cs[4 * u + 1] = v.y;
+                cs[4 * u + 2] = v.z;
+                cs[4 * u + 3] = v.w;
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const float c = pos_ok ? cs[2 * u] : 0.f, s = pos_ok ? cs[2 * u + 1] : 0.f;
+                const float a0 = ylo[u], b0 = yhi[u];
+                ylo[u] = fmaf(a0, c, -b0 * s);
+                yhi[u] = fmaf(a0, s, b0 * c);
+              }
+            }
+            uint4 plo, phi;
+            plo.x = pack_bf16x2(ylo[0], ylo[1]);
+            plo.y = pack_bf16x2(ylo[2], ylo[3]);
+            plo.z = pack_bf16x2(ylo[4], ylo[5]);
+            plo.w = pack_bf16x2(ylo[6], ylo[7]);
+            phi.x = pack_bf16x2(yhi[0], yhi[1]);
+            phi.y = pack_bf16x2(yhi[2], yhi[3]);
+            phi.z = pack_bf16x2(yhi[4], yhi[5]);
+            phi.w = pack_bf16x2(yhi[6], yhi[7]);
+            *reinterpret_cast<uint4*>(myrow + j0 * 2) = plo;
+            *reinterpret_cast<uint4*>(myrow + (H2 + j0) * 2) = phi;
+          }
+        }
+        if (hl == C::kHpt - 1) {
+          // Every TMEM read of this accumulator is done: the MMA warp may reuse it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_acc_empty[a]));
+        }
+        if (live) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.out[part], smem_u32(buf), head * D, row0);
+            bulk_commit();
+          }
+          ++nstore;
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_read_all();  // staging stays until every store has read it
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_qkv_d(const QkvArgs& a, int* drv_err, cudaStream_t stream) {
+  using C = QkvCfg<D>;
+  QkvMaps maps;
+  const uint64_t n = static_cast<uint64_t>(a.n);
+  const uint64_t hidden = static_cast<uint64_t>(a.hidden);
+  const uint64_t cols = 3ull * a.heads * D;
+  auto make = [&](CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box0,
+                  uint32_t box1, CUtensorMapSwizzle sw) -> bool {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {inner * 2};
+    const uint32_t box[2] = {box0, box1};
+    CUresult r = encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                   const_cast<void*>(base), dims, strides, box, sw);
+    if (r != CUDA_SUCCESS) {
+      *drv_err = static_cast<int>(r);
+      return false;
+    }
+    return true;
+  };
+  if (!make(&maps.x, a.x, hidden, n, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make(&maps.w, a.w, hidden, cols, kBK, C::kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make(&maps.out[0], a.q, (uint64_t)a.heads * D, n, D, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make(&maps.out[1], a.k, (uint64_t)a.heads * D, n, D, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make(&maps.out[2], a.v, (uint64_t)a.heads * D, n, D, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  QkvParams p;
+  p.bias = a.bias;
+  p.pos = a.positions;
+  p.cos_sin = reinterpret_cast<const float2*>(a.cos_sin);
+  p.dev_status = a.dev_status;
+  p.n = static_cast<int>(a.n);
+  p.heads = a.heads;
+  p.max_pos = a.max_pos;
+  p.tiles_n = static_cast<int>(cols / C::kBN);
+  const int64_t tiles_m = (a.n + kBM - 1) / kBM;
+  const int64_t n_tiles = tiles_m * p.tiles_n;
+  if (n_tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.k_steps = (a.hidden + kBK - 1) / kBK;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(n_tiles < sms ? n_tiles : sms);
+  e = cudaFuncSetAttribute(qkv_rope_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  qkv_rope_kernel<D><<<grid, kQkvThreads, C::kSmemBytes, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+// The cos/sin table: pair j of position p turns by p * base^(-2j/rot_dim). The angle
+// and its sine and cosine are taken in double precision and rounded to fp32 once.
+__global__ void rope_cache_kernel(float2* __restrict__ out, int max_pos, int rot_dim,
+                                  double base) {
+  const int half = rot_dim / 2;
+  const int64_t total = static_cast<int64_t>(max_pos) * half;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(i / half), j = static_cast<int>(i % half);
+    const double inv_freq = pow(base, -2.0 * j / rot_dim);
+    double s, c;
+    sincos(static_cast<double>(pos) * inv_freq, &s, &c);
+    out[i] = make_float2(static_cast<float>(c), static_cast<float>(s));
+  }
+}
+
+}  // namespace
+
+int qkv_heads_per_tile(int head_dim) {
+  switch (head_dim) {
+    case 64: return QkvCfg<64>::kHpt;
+    case 80: return QkvCfg<80>::kHpt;
+    case 128: return QkvCfg<128>::kHpt;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_qkv_rope(const QkvArgs& a, int* drv_err, cudaStream_t stream) {
+  switch (a.head_dim) {
+    case 64: return launch_qkv_d<64>(a, drv_err, stream);
+    case 80: return launch_qkv_d<80>(a, drv_err, stream);
+    case 128: return launch_qkv_d<128>(a, drv_err, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_rope_cache(int max_pos, int rot_dim, double base, float* cos_sin,
+                              cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(max_pos) * (rot_dim / 2);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  rope_cache_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<float2*>(cos_sin), max_pos, rot_dim, base);
+  return cudaGetLastError();
+}
+
+}  // namespace tts

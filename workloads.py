@@ -19,6 +19,11 @@ Named workloads (sizes from the pages):
            bf16 paged KV cache of 2590 tokens in pages of 64 with a shuffled page
            table, 2048 distinct indices per query inside its causal window,
            scale 1/sqrt(576); index permutations drawn with seeds 100..107.
+  vision_qkv  the projection in front of the vision attention: N = 8547 tokens,
+           hidden = 16 x 80 = 1280, x ~ N(0,1) and W ~ N(0, 1/hidden) in bf16 (so
+           q/k/v come out near unit variance), bias ~ N(0, 0.1^2) fp32, positions
+           0..N-1, cos/sin table over 32768 positions (the max_seq_len of the
+           SGLang write-up's RoPE table).
 """
 from __future__ import annotations
 
@@ -28,7 +33,7 @@ from dataclasses import dataclass, field
 import torch
 
 SEEDS = {"tiny": 0, "vision": 1, "varlen": 2, "topk": 3, "sparse": 4, "topk_long": 5,
-         "decode": 6}
+         "decode": 6, "vision_qkv": 7}
 PERM_SEEDS = tuple(range(100, 108))
 
 
@@ -249,3 +254,32 @@ def permute_rows(idx: torch.Tensor, seed: int) -> torch.Tensor:
     for r in range(idx.shape[0]):
         out[r] = idx[r, torch.randperm(idx.shape[1], generator=g)]
     return out
+
+
+@dataclass
+class QkvInputs:
+    x: torch.Tensor          # bf16 [n, hidden]
+    w: torch.Tensor          # bf16 [3 * heads * d, hidden]
+    bias: torch.Tensor       # fp32 [3 * heads * d] or None
+    positions: torch.Tensor  # int32 [n]
+    heads: int
+    d: int
+    max_pos: int
+    base: float = 10000.0
+
+    def flops(self) -> float:
+        """Algorithmic FLOPs of the projection: 2 per multiply-add of x W^T."""
+        n, hidden = self.x.shape
+        return 2.0 * n * hidden * self.w.shape[0]
+
+
+def vision_qkv_inputs(n=8547, heads=16, d=80, hidden=None, max_pos=32768, bias=True,
+                      positions=None, seed=None) -> QkvInputs:
+    g = _gen(SEEDS["vision_qkv"] if seed is None else seed)
+    hidden = heads * d if hidden is None else hidden
+    x = torch.randn(n, hidden, generator=g).to(torch.bfloat16)
+    w = (torch.randn(3 * heads * d, hidden, generator=g) / math.sqrt(hidden)).to(torch.bfloat16)
+    b = (0.1 * torch.randn(3 * heads * d, generator=g)) if bias else None
+    if positions is None:
+        positions = torch.arange(n, dtype=torch.int32)
+    return QkvInputs(x, w, b, positions.to(torch.int32), heads, d, max_pos)
