@@ -51,7 +51,7 @@ struct QkvCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 4 * 2 * kOutBytes + 1024;
   static_assert(kBN % 16 == 0 && kBN <= 256, "MMA N");
   static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
-  static_assert(kSmemBytes + 256 <= 232448, "shared memory");
+  static_assert(kSmemBytes + 256 + kBN * 4 <= 232448, "shared memory");
 };
 
 struct QkvMaps {
@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       bar_acc_empty[2], bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float4 s_bias[C::kBN / 4];  // the current tile's bias (epilogue)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -190,26 +191,36 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;  // TMEM lane quarter = rows q4*32 .. q4*32+31 of the tile
+    const int et = tid - 64;  // 0 .. 127 over the four epilogue warps
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     uint8_t* obuf[2] = {out_base + ((warp - 2) * 2) * C::kOutBytes,
                         out_base + ((warp - 2) * 2 + 1) * C::kOutBytes};
     int nstore = 0;  // heads staged so far by this warp (staging buffer = nstore & 1)
+    bool ok = true;
     int i = 0;
+    // Every epilogue warp runs every iteration (both named barriers included), also
+    // after a wait gave up, so the barriers always see all 128 threads.
     for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++i) {
       const int a = i & 1;
-      if (!warp_wait(smem_u32(&bar_acc_full[a]), (i >> 1) & 1, abort_flag, p.dev_status)) break;
-      tc_fence_after();
       const int tm = t / p.tiles_n, tn = t % p.tiles_n;
       const int row0 = tm * kBM + q4 * 32;  // this warp's first token
       const int row = row0 + lane;
       // A warp whose 32 rows all lie past the last token only frees the accumulator.
       const bool live = row0 < p.n;
       const int hh0 = tn * C::kHpt;  // first head column of the tile, in [0, 3H)
+      const bool any_rot = hh0 < 2 * p.heads;
+      // The tile's bias (BN values) goes to shared memory and the token's cos/sin row to
+      // registers while the MMAs of the tile still run.
+      named_barrier_sync(1, 128);  // every warp is done with the previous tile's bias
+      for (int c = et; c < C::kBN / 4; c += 128)
+        s_bias[c] = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias +
+                                                                    static_cast<int64_t>(hh0) * D) + c)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
       // Position of this thread's token; a position outside the table is reported,
       // and that token's q and k are written as zeros.
       int pos = 0;
       bool pos_ok = true;
-      if (live && row < p.n && hh0 < 2 * p.heads) {
+      if (ok && live && row < p.n && any_rot) {
         pos = p.pos[row];
         pos_ok = pos >= 0 && pos < p.max_pos;
         if (!pos_ok) {
@@ -223,17 +234,21 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       constexpr bool kCsRegs = D <= 80;
       float4 csr[kCsRegs ? H2 / 2 : 1];
       if constexpr (kCsRegs) {
-        if (live && hh0 < 2 * p.heads) {
+        if (ok && live && any_rot) {
 #pragma unroll
           for (int u = 0; u < H2 / 2; ++u) csr[u] = __ldg(cs4 + u);
         }
       }
+      named_barrier_sync(1, 128);  // the bias is in shared memory
+      ok = ok && warp_wait(smem_u32(&bar_acc_full[a]), (i >> 1) & 1, abort_flag, p.dev_status);
+      if (!ok) continue;
+      tc_fence_after();
 #pragma unroll 1
       for (int hl = 0; hl < C::kHpt; ++hl) {
         const int hh = hh0 + hl;
         const int part = hh / p.heads, head = hh - part * p.heads;
         const bool rot = part < 2;
-        const float* bias = p.bias ? p.bias + static_cast<int64_t>(hh) * D : nullptr;
+        const float4* b4 = s_bias + hl * (D / 4);
         const uint32_t tcol = lane_base + a * 256 + hl * D;
         uint8_t* buf = obuf[nstore & 1];
         // The store that last read this buffer (two stores ago) must be done reading.
@@ -241,29 +256,22 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
         __syncwarp();
         uint8_t* myrow = buf + lane * (D * 2);
         if (live) {
+          uint32_t r[D];  // the head's D accumulator columns of this row, one round trip
+#pragma unroll
+          for (int c = 0; c < D; c += 8)
+            tmem_ld8(tcol + c, *reinterpret_cast<uint32_t(*)[8]>(&r[c]));
+          tmem_ld_wait();
 #pragma unroll
           for (int j0 = 0; j0 < H2; j0 += 8) {
-            uint32_t lo[8], hi[8];
-            tmem_ld8(tcol + j0, lo);
-            tmem_ld8(tcol + H2 + j0, hi);
-            tmem_ld_wait();
             float ylo[8], yhi[8];
+            const float4 b0 = b4[j0 / 4], b1 = b4[j0 / 4 + 1];
+            const float4 c0 = b4[(H2 + j0) / 4], c1 = b4[(H2 + j0) / 4 + 1];
+            const float bl[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float bh[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              ylo[u] = __uint_as_float(lo[u]);
-              yhi[u] = __uint_as_float(hi[u]);
-            }
-            if (bias != nullptr) {
-              const float4* b4 = reinterpret_cast<const float4*>(bias);
-              const float4 b0 = __ldg(b4 + j0 / 4), b1 = __ldg(b4 + j0 / 4 + 1);
-              const float4 c0 = __ldg(b4 + (H2 + j0) / 4), c1 = __ldg(b4 + (H2 + j0) / 4 + 1);
-              const float bl[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-              const float bh[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                ylo[u] += bl[u];
-                yhi[u] += bh[u];
-              }
+              ylo[u] = __uint_as_float(r[j0 + u]) + bl[u];
+              yhi[u] = __uint_as_float(r[H2 + j0 + u]) + bh[u];
             }
             if (rot) {
               float cs[16];  // (cos, sin) of pairs j0 .. j0+7
