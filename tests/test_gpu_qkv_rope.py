@@ -91,6 +91,25 @@ def test_parity_random_positions(tts, n, heads, d, hidden, bias):
     assert torch.equal(q, q2) and torch.equal(k, k2) and torch.equal(v, v2)
 
 
+@pytest.mark.parametrize("n,heads,d,hidden", [
+    (1100, 16, 80, 256),   # 5 x 16 pair tiles: on a 152-SM GPU some pairs take two
+    (3300, 8, 64, 128),    # 13 x 6 pair tiles of 4 heads of 64
+])
+def test_parity_with_several_tiles_per_pair(tts, n, heads, d, hidden):
+    """More pair tiles than CTA pairs, so pairs run several tiles through both TMEM
+    accumulators and the stage ring wraps across tiles. Every row and head is compared."""
+    g = torch.Generator().manual_seed(n)
+    pos = torch.randint(0, 8547, (n,), generator=g, dtype=torch.int32)
+    inp = W.vision_qkv_inputs(n=n, heads=heads, d=d, hidden=hidden, max_pos=8547,
+                              positions=pos, seed=n + 1)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, k, v = gpu_run(tts, inp, status=st)
+    tts.check_status(st)
+    rq, rk, rv = oracle_run(inp)
+    for got, ref, name in ((q, rq, "q"), (k, rk, "k"), (v, rv, "v")):
+        check(got, ref, f"{name} n={n} H={heads} d={d}")
+
+
 def test_out_of_range_positions_are_zeroed_and_flagged(tts):
     n, heads, d = 200, 16, 80
     pos = torch.arange(n, dtype=torch.int32)
