@@ -24,6 +24,10 @@ arrays. Each function cites the passage of the pages it follows in that file:
   (j, j + d/2), angle pos * base^(-2j/d), base 10000 unless given.
 * ``round_bf16`` -- round-to-nearest-even of fp32 values to the bf16 grid, the
   rounding the CUDA path applies to fp32 inputs at its boundary.
+* ``round_e4m3`` / ``quant_e4m3`` / ``quant_fp8_prefill`` -- FP8 (e4m3) rounding and
+  block quantization of the prefill's q (one scale per token and head) and k (one scale
+  per KV head) ("从 SGLang Kernel源码到 GPU Trace", section 3.2; "AMD MI250部署", sections
+  4.1 and 5.3); the format and blocks are not on the pages: e4m3, scale = max|x| / 448.
 
 Pins (tests/test_oracle.py): closed forms (Q = 0, huge scale, causal row 0,
 identical keys, q = 0 / single index for sparse), invariants (rows of P sum to
@@ -82,6 +86,10 @@ def _load():
             lib.oracle_qkv_rope.restype = None
             lib.oracle_rope_cache.argtypes = [i32, i32, dbl, P]
             lib.oracle_rope_cache.restype = None
+            lib.oracle_round_e4m3.argtypes = [dbl]
+            lib.oracle_round_e4m3.restype = dbl
+            lib.oracle_quant_e4m3.argtypes = [P, i64, i64, P, P]
+            lib.oracle_quant_e4m3.restype = None
             _lib = lib
     return _lib
 
@@ -188,3 +196,42 @@ def rope_cache(max_pos: int, rot_dim: int, base: float = 10000.0):
     out = np.empty((max_pos, rot_dim // 2, 2), np.float64)
     _load().oracle_rope_cache(int(max_pos), int(rot_dim), float(base), _p(out))
     return out
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Nearest e4m3 value (ties to even, |x| > 448 clamped to 448), float64."""
+    a = np.asarray(x, dtype=np.float64)
+    f = _load().oracle_round_e4m3
+    return np.array([f(float(v)) for v in a.ravel()], dtype=np.float64).reshape(a.shape)
+
+
+def quant_e4m3(x, block_len: int):
+    """Quantize contiguous blocks of block_len values. Returns (scales float32 [nblocks],
+    codes float32 [same shape as x], the e4m3 values)."""
+    xf = _f32(x)
+    n = xf.size
+    assert block_len > 0 and n % block_len == 0
+    nb = n // block_len
+    scale = np.empty(nb, np.float32)
+    codes = np.empty(xf.shape, np.float32)
+    _load().oracle_quant_e4m3(_p(xf), nb, block_len, _p(scale), _p(codes))
+    return scale, codes
+
+
+def quant_fp8_prefill(q, k):
+    """The FP8 prefill's quantization of q [T, Hq, d] (one block per token and head) and
+    k [T, Hkv, d] (one block per KV head, over all tokens). Returns (q_codes, q_scale
+    [T, Hq], k_codes, k_scale [Hkv]) and the dequantized q and k (codes * scale, rounded
+    to float32 for the attention oracle)."""
+    q = _f32(q)
+    k = _f32(k)
+    tq, hq, d = q.shape
+    tk, hkv, _ = k.shape
+    qs, qc = quant_e4m3(q, d)
+    kt = np.ascontiguousarray(k.transpose(1, 0, 2))          # [Hkv, T, d]
+    ks, kct = quant_e4m3(kt, max(tk, 1) * d) if tk > 0 else (np.ones(hkv, np.float32), kt)
+    kc = np.ascontiguousarray(kct.transpose(1, 0, 2))
+    qs = qs.reshape(tq, hq)
+    qd = (qc.astype(np.float64) * qs[:, :, None]).astype(np.float32)
+    kd = (kc.astype(np.float64) * ks[None, :, None]).astype(np.float32)
+    return qc, qs, kc, ks, qd, kd

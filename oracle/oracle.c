@@ -333,3 +333,51 @@ void oracle_rope_cache(int max_pos, int rot_dim, double base, double* out) {
       out[((int64_t)p * (rot_dim / 2) + j) * 2 + 1] = sin(ang);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* O5. FP8 (e4m3) block quantization for the prefill QK^T product            */
+/* ("从 SGLang Kernel源码到 GPU Trace", section 3.2: part of the prefill runs  */
+/* in FP8; "AMD MI250部署DeepSeek-V4-Flash", section 4.1: matmul inputs may   */
+/* be FP8 with FP32 accumulation, section 5.3: FP8 by block quantization).    */
+/* The pages fix neither the format nor the blocks; the reading taken: e4m3  */
+/* (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities, */
+/* largest finite value 1.75 * 2^8 = 448, smallest normal 2^-6, subnormals   */
+/* j * 2^-9), one fp32 scale per block = (block's max |x|) / 448 in fp32.     */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest e4m3 value of x, ties to the even mantissa, magnitudes beyond 448  */
+/* clamped to 448. The grid spacing in the binade [2^e, 2^(e+1)) is          */
+/* 2^(e-3) for e >= -6, and 2^-9 below 2^-6 (subnormals).                    */
+double oracle_round_e4m3(double x) {
+  const double a = fabs(x);
+  if (a == 0.0) return x;
+  int e;
+  frexp(a, &e); /* a = f * 2^e, f in [0.5, 1): binade [2^(e-1), 2^e) */
+  int eb = e - 1;
+  if (eb < -6) eb = -6;
+  const double ulp = ldexp(1.0, eb - 3);
+  double r = nearbyint(a / ulp) * ulp; /* default rounding mode: to nearest, ties to even */
+  if (r > 448.0) r = 448.0;
+  return x < 0 ? -r : r;
+}
+
+/* Quantize nblocks contiguous blocks of len values: scale[b] = max|x| / 448   */
+/* (fp32; 1 for an all-zero block), code = e4m3(x / scale[b]) with the        */
+/* division in fp32 (the precision in which the CUDA path takes the same      */
+/* decision). codes receives the e4m3 values as floats (exactly).             */
+void oracle_quant_e4m3(const float* x, int64_t nblocks, int64_t len, float* scale, float* codes) {
+  for (int64_t b = 0; b < nblocks; ++b) {
+    const float* xb = x + b * len;
+    float amax = 0.f;
+    for (int64_t i = 0; i < len; ++i) {
+      const float v = fabsf(xb[i]);
+      if (v > amax) amax = v;
+    }
+    const float s = amax > 0.f ? amax / 448.0f : 1.0f;
+    scale[b] = s;
+    for (int64_t i = 0; i < len; ++i) {
+      const float y = xb[i] / s;
+      codes[b * len + i] = (float)oracle_round_e4m3((double)y);
+    }
+  }
+}

@@ -451,3 +451,95 @@ def test_rope_cache_rows_are_powers_of_the_first():
     p = np.arange(300)[:, None]
     np.testing.assert_allclose(z, np.power(z[1][None, :], p), atol=1e-11)
     np.testing.assert_allclose(np.abs(z), 1.0, atol=1e-15)
+
+
+# ---- FP8 (e4m3) rounding and block quantization ----------------------------------------
+
+def _e4m3_table():
+    """Every finite e4m3 value with its code, decoded from the bit layout (sign, 4
+    exponent bits with bias 7, 3 mantissa bits; exponent field 0 = subnormal; the code
+    with all exponent and mantissa bits set is NaN)."""
+    vals, codes = [], []
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            continue
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append(-v if s else v)
+        codes.append(c)
+    return np.array(vals), np.array(codes)
+
+
+def _nearest_e4m3(x, vals, codes):
+    """Brute force: the nearest table value; ties to the even code; beyond 448 -> 448."""
+    out = []
+    for v in x:
+        d = np.abs(vals - v)
+        best = np.flatnonzero(d == d.min())
+        if len(best) > 1:
+            best = [b for b in best if codes[b] % 2 == 0] or best
+        out.append(vals[best[0]])
+    return np.array(out)
+
+
+def test_e4m3_rounding_matches_brute_force_nearest():
+    vals, codes = _e4m3_table()
+    assert vals.max() == 448.0 and np.min(vals[vals > 0]) == 2.0 ** -9
+    # every representable value maps to itself
+    np.testing.assert_array_equal(oracle.round_e4m3(vals), vals)
+    rng = np.random.default_rng(40)
+    x = np.concatenate([
+        rng.standard_normal(3000) * 2.0 ** rng.integers(-12, 9, 3000),   # all binades
+        (vals[:-1] + vals[1:]) / 2,                                       # exact midpoints
+        rng.uniform(-448, 448, 500),
+    ])
+    x = x.astype(np.float32).astype(np.float64)   # the oracle rounds fp32 values
+    inside = np.abs(x) <= 448
+    np.testing.assert_array_equal(oracle.round_e4m3(x[inside]),
+                                  _nearest_e4m3(x[inside], vals, codes))
+    # saturation: beyond the largest finite value the magnitude clamps to 448
+    big = np.array([448.0, 449.0, 463.9, 464.0, 1e6, -500.0, -1e30])
+    np.testing.assert_array_equal(oracle.round_e4m3(big), np.sign(big) * 448.0)
+
+
+def test_e4m3_rounding_matches_torch_float8():
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal(20000) * 2.0 ** rng.integers(-12, 9, 20000)).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    lib = torch.from_numpy(x).to(f8).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_e4m3(x.astype(np.float64)), lib)
+
+
+def test_block_quantization_scales_and_error_bound():
+    rng = np.random.default_rng(42)
+    x = (rng.standard_normal((50, 128)) * np.exp(rng.uniform(-6, 4, (50, 1)))).astype(np.float32)
+    x[7] = 0.0                                              # an all-zero block
+    s, c = oracle.quant_e4m3(x, 128)
+    assert s[7] == 1.0 and not c[7].any()
+    amax = np.abs(x).max(axis=1)
+    nz = amax > 0
+    np.testing.assert_array_equal(s[nz], (amax[nz] / np.float32(448)).astype(np.float32))
+    # the largest element of every block lands on +-448, and no code exceeds it
+    assert np.all(np.abs(c).max(axis=1)[nz] == 448.0) and np.abs(c).max() <= 448.0
+    # dequantized values are within half a grid step of x (relative 2^-4 for normal
+    # values, 2^-10 of the scale in the subnormal range)
+    deq = c.astype(np.float64) * s[:, None]
+    bound = 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s[:, None] + 1e-30
+    assert np.all(np.abs(deq - x) <= bound * (1 + 1e-6))
+
+
+def test_fp8_prefill_quantization_blocks():
+    rng = np.random.default_rng(43)
+    q = rng.standard_normal((37, 4, 128)).astype(np.float32)
+    k = (rng.standard_normal((37, 2, 128)) * np.array([1.0, 30.0])[None, :, None]).astype(np.float32)
+    qc, qs, kc, ks, qd, kd = oracle.quant_fp8_prefill(q, k)
+    assert qs.shape == (37, 4) and ks.shape == (2,)
+    # q: one scale per token and head; k: one scale per KV head over every token
+    np.testing.assert_array_equal(qs, (np.abs(q).max(axis=2) / np.float32(448)).astype(np.float32))
+    np.testing.assert_array_equal(ks, (np.abs(k).max(axis=(0, 2)) / np.float32(448)).astype(np.float32))
+    np.testing.assert_allclose(kd[:, 1], kc[:, 1] * ks[1], rtol=1e-7)
+    # the dequantized tensors stay within the e4m3 half-step of the inputs
+    assert np.all(np.abs(qd - q) <= 2.0 ** -4 * np.abs(q) + 2.0 ** -10 * qs[:, :, None] + 1e-6)
