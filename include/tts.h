@@ -254,6 +254,59 @@ tts_status tts_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
 size_t tts_sparse_workspace_bytes(int32_t nq);
 
 /*
+ * FP8 (e4m3) block quantization of the prefill's q and k, for tts_attn_fwd_varlen_fp8.
+ *
+ * "从 SGLang Kernel源码到 GPU Trace" (section 3.2) runs part of the prefill in FP8; "AMD
+ * MI250部署DeepSeek-V4-Flash" allows FP8 matmul inputs with FP32 accumulation (section
+ * 4.1) and quantizes by blocks (section 5.3). The pages fix neither the format nor the
+ * blocks; the reading taken: e4m3 (largest finite value 448), one block per (token,
+ * head) row of q and one block per KV head of k (all its tokens), scale = max|x| / 448
+ * in fp32 (1 for an all-zero block), code = e4m3(x / scale) with the division in fp32
+ * and the conversion to nearest, ties to even, saturating at +-448.
+ *
+ * q        device bf16 [total_q, num_heads_q, head_dim]
+ * k        device bf16 [total_k, num_heads_kv, head_dim]
+ * q8, k8   device e4m3 codes, one byte per value, same layouts, written
+ * q_scale  device fp32 [total_q, num_heads_q], written
+ * k_scale  device fp32 [num_heads_kv], written (it also holds the per-head maxima
+ *          between the launches this call enqueues)
+ * head_dim a multiple of 4; num_heads_kv <= 4096; all pointers 16-byte aligned; a
+ * zero-sized q (or k) may come with null pointers for its tensors. Deterministic: the
+ * per-head maxima are reduced with integer atomics on the bits of |x|.
+ */
+tts_status tts_quantize_fp8_prefill(const void* q, int64_t total_q, int32_t num_heads_q,
+                                   const void* k, int64_t total_k, int32_t num_heads_kv,
+                                   int32_t head_dim, void* q8, float* q_scale, void* k8,
+                                   float* k_scale, void* stream);
+
+/*
+ * Dense attention forward with FP8 (e4m3) q and k in the S = Q K^T product.
+ *
+ * As tts_attn_fwd_varlen (same sequences, masks, layouts of v / out / lse, workspace of
+ * tts_attn_workspace_bytes(..., TTS_BF16) bytes, device checks and errors), except that
+ * q and k arrive as e4m3 codes with the scales of tts_quantize_fp8_prefill, and the
+ * scores are
+ *   s_j = scale * q_scale[i, h] * k_scale[g] * sum_t q8[i,h,t] k8[j,g,t]
+ * computed by e4m3 x e4m3 tensor-core products accumulated in fp32. The softmax
+ * statistics stay fp32 and P V stays bf16 x bf16 with fp32 accumulation, as the
+ * precision table of "AMD MI250部署DeepSeek-V4-Flash" (section 4.1) keeps the softmax
+ * path and P V. head_dim must be 128 (else TTS_ERR_UNSUPPORTED).
+ *
+ * q8      device e4m3 [total_q, num_heads_q, 128]     q_scale device fp32 [total_q, num_heads_q]
+ * k8      device e4m3 [total_k, num_heads_kv, 128]    k_scale device fp32 [num_heads_kv]
+ * v       device bf16 [total_k, num_heads_kv, 128]
+ */
+tts_status tts_attn_fwd_varlen_fp8(const void* q8, const float* q_scale, const void* k8,
+                                   const float* k_scale, const void* v, int64_t total_q,
+                                   int64_t total_k, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int32_t batch,
+                                   int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                   int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+                                   int32_t causal, float scale, float* out, float* lse,
+                                   void* workspace, size_t workspace_bytes,
+                                   uint32_t* dev_status, void* stream);
+
+/*
  * cos/sin table of rotary position embedding, built once and read by tts_qkv_rope.
  *
  * The position-indexed table of "从 SGLang Kernel源码到 GPU Trace" (section 3.3: cos

@@ -223,3 +223,33 @@ def test_rope_cache_host_validation(L):
     assert f(10, 80, float("inf"), A, NUL) == tts.TTS_ERR_INVALID_ARG
     assert f(10, 80, 10000.0, NUL, NUL) == tts.TTS_ERR_INVALID_ARG
     assert f(10, 80, 10000.0, ctypes.c_void_p(0x10004), NUL) == tts.TTS_ERR_INVALID_ARG
+
+
+def test_fp8_prefill_host_validation(L):
+    import tiled_top_sparse_gb300 as tts
+    A = ctypes.c_void_p(0x10000)
+    f = L.tts_attn_fwd_varlen_fp8
+    ok = [A, A, A, A, A, 256, 256, A, A, 1, 256, 256, 4, 2, 128, 1, 0.1, A, A, A, 256, NUL, NUL]
+
+    def call(i=None, val=None):
+        args = list(ok)
+        if i is not None:
+            args[i] = val
+        return f(*args)
+
+    for i in (0, 1, 2, 3, 4, 7, 8, 17):
+        assert call(i, NUL) == tts.TTS_ERR_INVALID_ARG, i
+    assert call(14, 64) == tts.TTS_ERR_UNSUPPORTED         # e4m3 path: head_dim 128 only
+    assert call(13, 3) == tts.TTS_ERR_INVALID_ARG          # 4 q heads over 3 KV heads
+    assert call(16, -1.0) == tts.TTS_ERR_INVALID_ARG
+    assert call(15, 2) == tts.TTS_ERR_INVALID_ARG
+    assert call(19, NUL) == tts.TTS_ERR_WORKSPACE
+    assert call(20, 16) == tts.TTS_ERR_WORKSPACE
+    assert call(5, 0) == tts.TTS_OK                        # nothing to compute
+    g = L.tts_quantize_fp8_prefill
+    okq = [A, 10, 4, A, 10, 2, 128, A, A, A, A, NUL]
+    for i, bad in ((1, -1), (2, 0), (5, 0), (6, 126), (10, NUL), (10, ctypes.c_void_p(0x10004)),
+                   (0, NUL), (7, NUL), (8, NUL), (3, NUL), (9, NUL)):
+        args = list(okq)
+        args[i] = bad
+        assert g(*args) == tts.TTS_ERR_INVALID_ARG, i

@@ -9,6 +9,10 @@ no fallback: if the library is missing or fails to load, calls raise.
     topk_select(logits, row_starts, row_lens, k, idx=None, status=None)
     sparse_attn_paged(q, kv_cache, page_table, idx, kv_len, scale, dv=512,
                       out=None, lse=None, status=None)
+    quantize_fp8_prefill(q, k)
+    attn_fwd_varlen_fp8(q8, q_scale, k8, k_scale, v, cu_seqlens_q, cu_seqlens_k,
+                        max_seqlen_q, max_seqlen_k, causal, scale, out=None, lse=None,
+                        workspace=None, status=None)
     rope_cache(max_pos, rot_dim, base=10000.0, out=None, device=None)
     qkv_rope(x, w, bias, positions, cos_sin, num_heads, q=None, k=None, v=None,
              status=None)
@@ -53,6 +57,8 @@ EXPORTED = (
     "tts_sparse_workspace_bytes",
     "tts_sparse_attn_decode",
     "tts_paged_kv_write",
+    "tts_quantize_fp8_prefill",
+    "tts_attn_fwd_varlen_fp8",
     "tts_rope_cache",
     "tts_qkv_rope",
     "tts_attn_fwd_varlen_f32_noalloc",
@@ -105,6 +111,11 @@ def lib() -> ctypes.CDLL:
     L.tts_paged_kv_write.restype = ctypes.c_int
     L.tts_sparse_workspace_bytes.argtypes = [i32]
     L.tts_sparse_workspace_bytes.restype = ctypes.c_size_t
+    L.tts_quantize_fp8_prefill.argtypes = [P, i64, i32, P, i64, i32, i32, P, P, P, P, P]
+    L.tts_quantize_fp8_prefill.restype = ctypes.c_int
+    L.tts_attn_fwd_varlen_fp8.argtypes = [P, P, P, P, P, i64, i64, P, P, i32, i32, i32, i32,
+                                          i32, i32, i32, f32, P, P, P, ctypes.c_size_t, P, P]
+    L.tts_attn_fwd_varlen_fp8.restype = ctypes.c_int
     L.tts_rope_cache.argtypes = [i32, i32, f32, P, P]
     L.tts_rope_cache.restype = ctypes.c_int
     L.tts_qkv_rope.argtypes = [P, i64, i32, P, P, P, P, i32, i32, i32, P, P, P, P, P]
@@ -407,3 +418,64 @@ def qkv_rope(x, w, bias, positions, cos_sin, num_heads, q=None, k=None, v=None, 
                               _ptr(outs[1]), _ptr(outs[2]), _ptr(status), _stream(x.device))
     _check(code, "tts_qkv_rope")
     return tuple(outs)
+
+
+def quantize_fp8_prefill(q, k, q8=None, q_scale=None, k8=None, k_scale=None):
+    """e4m3 block quantization (tts_quantize_fp8_prefill) of q bf16 [Tq, Hq, d] (scale per
+    token and head) and k bf16 [Tk, Hkv, d] (scale per KV head). Returns (q8, q_scale, k8,
+    k_scale): codes as uint8 tensors of the input shapes (view them as
+    torch.float8_e4m3fn to read values), scales fp32 [Tq, Hq] and [Hkv]."""
+    _cuda_contig(q, "q", torch.bfloat16)
+    _cuda_contig(k, "k", torch.bfloat16)
+    _need(q.dim() == 3 and k.dim() == 3 and q.shape[2] == k.shape[2], "q, k [tokens, heads, d]")
+    tq, hq, d = q.shape
+    tk, hkv, _ = k.shape
+    dev = q.device
+    q8 = torch.empty((tq, hq, d), dtype=torch.uint8, device=dev) if q8 is None else q8
+    k8 = torch.empty((tk, hkv, d), dtype=torch.uint8, device=dev) if k8 is None else k8
+    q_scale = torch.empty((tq, hq), dtype=torch.float32, device=dev) if q_scale is None else q_scale
+    k_scale = torch.empty((hkv,), dtype=torch.float32, device=dev) if k_scale is None else k_scale
+    for t, n, dt in ((q8, "q8", torch.uint8), (k8, "k8", torch.uint8),
+                     (q_scale, "q_scale", torch.float32), (k_scale, "k_scale", torch.float32)):
+        _cuda_contig(t, n, dt)
+    code = lib().tts_quantize_fp8_prefill(_ptr(q), tq, hq, _ptr(k), tk, hkv, d, _ptr(q8),
+                                          _ptr(q_scale), _ptr(k8), _ptr(k_scale),
+                                          _stream(dev))
+    _check(code, "tts_quantize_fp8_prefill")
+    return q8, q_scale, k8, k_scale
+
+
+def attn_fwd_varlen_fp8(q8, q_scale, k8, k_scale, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                        max_seqlen_k, causal, scale, out=None, lse=None, workspace=None,
+                        status=None, want_lse=True):
+    """Dense attention with e4m3 q / k in Q K^T (tts_attn_fwd_varlen_fp8). q8 / k8 uint8
+    codes [T, H, 128] with their scales from quantize_fp8_prefill, v bf16. Returns (out
+    fp32 [Tq, Hq, 128], lse fp32 [Tq, Hq])."""
+    _cuda_contig(q8, "q8", torch.uint8)
+    _cuda_contig(k8, "k8", torch.uint8)
+    _cuda_contig(q_scale, "q_scale", torch.float32)
+    _cuda_contig(k_scale, "k_scale", torch.float32)
+    _cuda_contig(v, "v", torch.bfloat16)
+    _cuda_contig(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _cuda_contig(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+    _need(q8.dim() == 3 and k8.shape == v.shape, "q8 [Tq, Hq, d]; k8, v [Tk, Hkv, d]")
+    total_q, hq, d = q8.shape
+    total_k, hkv, _ = k8.shape
+    _need(tuple(q_scale.shape) == (total_q, hq) and k_scale.numel() == hkv, "scale shapes")
+    batch = cu_seqlens_q.numel() - 1
+    _need(batch >= 1 and cu_seqlens_k.numel() == batch + 1, "cu_seqlens sizes must be batch+1")
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=torch.float32, device=q8.device)
+    _cuda_contig(out, "out", torch.float32)
+    if lse is None and want_lse:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q8.device)
+    need = attn_workspace_bytes(total_q, total_k, hq, hkv, d, torch.bfloat16)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q8.device)
+    code = lib().tts_attn_fwd_varlen_fp8(
+        _ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(v), total_q, total_k,
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, int(max_seqlen_q), int(max_seqlen_k), hq,
+        hkv, d, int(bool(causal)), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(q8.device))
+    _check(code, "tts_attn_fwd_varlen_fp8")
+    return out, lse

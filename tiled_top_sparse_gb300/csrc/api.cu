@@ -323,6 +323,78 @@ tts_status tts_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
                                          dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+tts_status tts_quantize_fp8_prefill(const void* q, int64_t total_q, int32_t num_heads_q,
+                                   const void* k, int64_t total_k, int32_t num_heads_kv,
+                                   int32_t head_dim, void* q8, float* q_scale, void* k8,
+                                   float* k_scale, void* stream) {
+  if (total_q < 0 || total_k < 0 || num_heads_q < 1 || num_heads_kv < 1 ||
+      num_heads_kv > 4096 || head_dim < 4 || head_dim % 4 != 0)
+    return TTS_ERR_INVALID_ARG;
+  if (k_scale == nullptr || !aligned16(k_scale)) return TTS_ERR_INVALID_ARG;
+  if (total_q > 0 && (q == nullptr || q8 == nullptr || q_scale == nullptr || !aligned16(q) ||
+                      !aligned16(q8) || !aligned16(q_scale)))
+    return TTS_ERR_INVALID_ARG;
+  if (total_k > 0 && (k == nullptr || k8 == nullptr || !aligned16(k) || !aligned16(k8)))
+    return TTS_ERR_INVALID_ARG;
+  return from_cuda(launch_quant_fp8_prefill(q, total_q, num_heads_q, k, total_k, num_heads_kv,
+                                            head_dim, q8, q_scale, k8, k_scale,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+tts_status tts_attn_fwd_varlen_fp8(const void* q8, const float* q_scale, const void* k8,
+                                   const float* k_scale, const void* v, int64_t total_q,
+                                   int64_t total_k, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int32_t batch,
+                                   int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                   int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+                                   int32_t causal, float scale, float* out, float* lse,
+                                   void* workspace, size_t workspace_bytes,
+                                   uint32_t* dev_status, void* stream) {
+  if (q8 == nullptr || q_scale == nullptr || k8 == nullptr || k_scale == nullptr ||
+      v == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || out == nullptr)
+    return TTS_ERR_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+      num_heads_q < 1 || num_heads_kv < 1 || head_dim < 1)
+    return TTS_ERR_INVALID_ARG;
+  if (num_heads_q % num_heads_kv != 0) return TTS_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return TTS_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return TTS_ERR_INVALID_ARG;
+  if (head_dim != 128) return TTS_ERR_UNSUPPORTED;
+  if (total_q > 0x7FFFFF00LL || total_k > 0x7FFFFF00LL) return TTS_ERR_UNSUPPORTED;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(out))
+    return TTS_ERR_INVALID_ARG;
+  if (total_q == 0 || max_seqlen_q == 0) return TTS_OK;  // nothing to compute
+  if (workspace == nullptr || workspace_bytes < kCounterBytes || !aligned16(workspace))
+    return TTS_ERR_WORKSPACE;
+  AttnArgs a;
+  a.q = q8;
+  a.k = k8;
+  a.v = v;
+  a.fp8 = true;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.work_counter = static_cast<uint32_t*>(workspace);
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.batch = batch;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.hq = num_heads_q;
+  a.hkv = num_heads_kv;
+  a.d = head_dim;
+  a.causal = causal;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  int drv = 0;
+  cudaError_t e = launch_attn_fwd(a, &drv, static_cast<cudaStream_t>(stream));
+  if (drv != 0) return TTS_ERR_CUDA;
+  return from_cuda(e);
+}
+
 tts_status tts_rope_cache(int32_t max_pos, int32_t rot_dim, float base, float* cos_sin,
                           void* stream) {
   if (cos_sin == nullptr || !aligned16(cos_sin)) return TTS_ERR_INVALID_ARG;

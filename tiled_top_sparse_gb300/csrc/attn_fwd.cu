@@ -42,29 +42,51 @@ constexpr int kAttnThreads = 384;
 constexpr int kBlockM = 128;  // query rows per softmax warpgroup
 constexpr int kBlockN = 128;  // keys per K/V tile
 
-template <int D>
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0), fp32 D,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// D[tmem] (+)= A[smem] * B[smem], e4m3 operands, from the elected lane of a converged warp.
+__device__ __forceinline__ void mma_ss_f8_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate,
+                                                uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+      : "memory");
+}
+
+// F8: q and k are e4m3 (one byte per value) and S = Q K^T runs as kind::f8f6f4 MMAs;
+// V, P and O stay bf16 / fp32. Built for D = 128 only.
+template <int D, bool F8 = false>
 struct AttnCfg {
-  static constexpr int kMainBoxes = D / 64;  // 64-column SW128 boxes
-  static constexpr int kTail = D % 64;       // 0 or 16 (SW32 box)
+  static constexpr int kQKCols = F8 ? 128 : 64;  // q / k values per 128-byte row
+  static constexpr int kMainBoxes = D / kQKCols;  // SW128 boxes of q / k
+  static constexpr int kTail = F8 ? 0 : D % 64;   // 0 or 16 (SW32 box)
   static constexpr int kBoxBytes = kBlockN * 128;  // one SW128 box of 128 rows
   static constexpr int kTailBytes = kBlockN * 32;  // one SW32 box of 128 rows
   static constexpr int kTileBytes = kMainBoxes * kBoxBytes + (kTail ? kTailBytes : 0);
   // V for d=80 is loaded as three 32-column SW64 boxes (d 80..95 zero-filled by the
   // tensor map's bounds) so that one N=96 MMA per K step covers it; d=64/128 reuse the
   // K/Q layout.
-  static constexpr int kVBoxes = kTail ? 3 : kMainBoxes;
+  static constexpr int kVBoxes = kTail ? 3 : D / 64;
   static constexpr int kVBoxBytes = kTail ? kBlockN * 64 : kBoxBytes;
   static constexpr int kVTileBytes = kVBoxes * kVBoxBytes;
   static constexpr int kPvN = kTail ? 96 : D;
-  static constexpr int kStages = (D <= 80) ? 3 : 2;
+  static constexpr int kStages = (D <= 80 || F8) ? 3 : 2;
   static constexpr int kStageBytes = 8 * 4096;  // output staging, 4 KB per softmax warp
   static constexpr int kSmemBytes =
       (2 + kStages) * kTileBytes + kStages * kVTileBytes + kStageBytes + 1024;
   static_assert(kTail == 0 || kTail == 16, "head_dim must be 64, 80 or 128");
+  static_assert(!F8 || D == 128, "the e4m3 q / k path is built for head_dim 128");
 };
 
 struct AttnMaps {
-  CUtensorMap q, k, v;           // SW128 boxes {64, 1, 128}
+  CUtensorMap q, k, v;           // SW128 boxes {64, 1, 128} (q / k e4m3: {128, 1, 128})
   CUtensorMap q_t, k_t;          // SW32 boxes {16, 1, 128} for the d=64..79 tail
   CUtensorMap v_t;               // d=80: SW64 boxes {32, 1, 128} for all of V
 };
@@ -80,17 +102,19 @@ struct AttnParams {
   int64_t total_q, total_k;
   int batch, max_seqlen_q, max_seqlen_k, hq, hkv, causal, pairs_max;
   float scale, scale_log2;
+  const float* q_scale;  // e4m3 path: [total_q, hq] per (token, head)
+  const float* k_scale;  // e4m3 path: [hkv] per KV head
 };
 
-// Load one 128-row tile (all boxes) of a [tokens, heads, D] tensor.
-template <int D>
+// Load one 128-row tile (all boxes) of a [tokens, heads, D] tensor (F8: of e4m3 q / k).
+template <int D, bool F8 = false>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* main,
                                           const CUtensorMap* tail, uint32_t bar, int head,
                                           int token) {
-  using C = AttnCfg<D>;
+  using C = AttnCfg<D, F8>;
 #pragma unroll
   for (int b = 0; b < C::kMainBoxes; ++b)
-    tma_load_3d(dst + b * C::kBoxBytes, main, bar, b * 64, head, token);
+    tma_load_3d(dst + b * C::kBoxBytes, main, bar, b * C::kQKCols, head, token);
   if constexpr (C::kTail != 0)
     tma_load_3d(dst + C::kMainBoxes * C::kBoxBytes, tail, bar, C::kMainBoxes * 64, head, token);
 }
@@ -99,15 +123,20 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* main,
 // descriptors of the tiles' first box; every other K step is a constant offset
 // (the 14-bit start-address field never carries: shared addresses are < 256 KB).
 // e: the elected lane of the converged issuing warp.
-template <int D>
+// F8: e4m3 x e4m3 -> fp32, K = 32 per MMA, so the same 32-byte steps cover the row.
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_d, uint64_t k_d,
                                          uint64_t q_tail_d, uint64_t k_tail_d, uint32_t e) {
-  using C = AttnCfg<D>;
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kBlockN, 0, 0);
+  using C = AttnCfg<D, F8>;
+  constexpr uint32_t idesc =
+      F8 ? idesc_e4m3_f32(128, kBlockN) : idesc_bf16_f32(128, kBlockN, 0, 0);
 #pragma unroll
   for (int ks = 0; ks < C::kMainBoxes * 4; ++ks) {
     const uint32_t off = ((ks / 4) * C::kBoxBytes + (ks % 4) * 32) >> 4;
-    mma_ss_elect(d_tmem, q_d + off, k_d + off, idesc, ks > 0, e);
+    if constexpr (F8)
+      mma_ss_f8_elect(d_tmem, q_d + off, k_d + off, idesc, ks > 0, e);
+    else
+      mma_ss_elect(d_tmem, q_d + off, k_d + off, idesc, ks > 0, e);
   }
   if constexpr (C::kTail != 0) mma_ss_elect(d_tmem, q_tail_d, k_tail_d, idesc, 1, e);
 }
@@ -185,10 +214,10 @@ __device__ __forceinline__ bool decode_item(const AttnParams& p, int it, Item& w
 // Per CTA, items flow through a two-slot ring (producer -> MMA warp + softmax warps);
 // barrier phases run on counters that continue across items: gt = K/V tiles so far
 // (ring slots, S / P phases), nq = items with at least one tile (Q, O phases).
-template <int D>
+template <int D, bool F8 = false>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p) {
-  using C = AttnCfg<D>;
+  using C = AttnCfg<D, F8>;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   // bar_k / bar_v: K and V of a tile landed. With three stages (d <= 80) the V load
@@ -268,7 +297,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int tok = (int)(w.k_start + (int64_t)j * kBlockN);
         const uint32_t bk = smem_u32(&bar_k[st]);
         mbar_arrive_expect_tx(bk, kOneKV ? C::kTileBytes + C::kVTileBytes : C::kTileBytes);
-        load_tile<D>(sK(st), &maps.k, &maps.k_t, bk, w.g, tok);
+        load_tile<D, F8>(sK(st), &maps.k, &maps.k_t, bk, w.g, tok);
         last_k[st] = gj;
         return true;
       };
@@ -330,7 +359,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           const uint32_t bq = smem_u32(&bar_q[wq]);
           mbar_arrive_expect_tx(bq, C::kTileBytes);
-          load_tile<D>(sQ[wq], &maps.q, &maps.q_t, bq, w.h,
+          load_tile<D, F8>(sQ[wq], &maps.q, &maps.q_t, bq, w.h,
                        (int)(w.q_start + w.q_lo + wq * kBlockM));
           q_armed[wq] = nq + 1;
         }
@@ -393,7 +422,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (n0 > 0) {
-        issue_qk<D>(S_t[0], qd[0], kd[st0], qtd[0], ktd[st0], e);
+        issue_qk<D, F8>(S_t[0], qd[0], kd[st0], qtd[0], ktd[st0], e);
         mma_commit_elect(smem_u32(&bar_s[0]), e);
       }
       if (n0 <= 1) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
@@ -401,7 +430,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (n1 > 0) {
-        issue_qk<D>(S_t[1], qd[1], kd[st0], qtd[1], ktd[st0], e);
+        issue_qk<D, F8>(S_t[1], qd[1], kd[st0], qtd[1], ktd[st0], e);
         mma_commit_elect(smem_u32(&bar_s[1]), e);
       }
       if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st0]), e);
@@ -431,7 +460,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc_fence_after();
-        issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
+        issue_qk<D, F8>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
         mma_commit_elect(smem_u32(&bar_s[0]), e);
         if (j + 2 == n0) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
         if (!warp_wait(smem_u32(&bar_p[1]), (g1 + j) & 1, abort_flag, p.dev_status)) {
@@ -441,7 +470,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         issue_pv<D>(O_t[1], S_t[1], vd[st], j > 0, e);
         mma_commit_elect(smem_u32(&bar_kv_empty[st]), e);
-        issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
+        issue_qk<D, F8>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
         mma_commit_elect(smem_u32(&bar_s[1]), e);
         if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
         if (j + 2 == n1) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
@@ -471,7 +500,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               break;
             }
             tc_fence_after();
-            issue_qk<D>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
+            issue_qk<D, F8>(S_t[0], qd[0], kd[st1], qtd[0], ktd[st1], e);
             mma_commit_elect(smem_u32(&bar_s[0]), e);
             if (!kOneKV && !more1) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
             if (j + 2 == n0) mma_commit_elect(smem_u32(&bar_q_empty[0]), e);
@@ -497,7 +526,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               break;
             }
             tc_fence_after();
-            issue_qk<D>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
+            issue_qk<D, F8>(S_t[1], qd[1], kd[st1], qtd[1], ktd[st1], e);
             mma_commit_elect(smem_u32(&bar_s[1]), e);
             if (!kOneKV) mma_commit_elect(smem_u32(&bar_k_empty[st1]), e);
             if (j + 2 == n1) mma_commit_elect(smem_u32(&bar_q_empty[1]), e);
@@ -522,7 +551,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t S_row = tmem + wg * 128 + lane_off;
     const uint32_t O_row = tmem + 256 + wg * 128 + lane_off;
     float4* stage = reinterpret_cast<float4*>(stage_base + (warp - 4) * 4096);
-    const float c = p.scale_log2;
     int ni = 0, nq = 0, gt = 0;
     bool ok = true;
     while (ok) {
@@ -545,6 +573,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (p.causal) {
         const int64_t lim = i + (Lk - Lq) + 1;
         limit = lim < limit ? lim : limit;
+      }
+      // exp2-domain factor and natural scale of this row's scores; the e4m3 path folds
+      // in the row's q scale and the KV head's k scale (S is a product of codes).
+      float c = p.scale_log2, sc = p.scale;
+      if constexpr (F8) {
+        const float f =
+            ((i >= 0 && i < Lq) ? p.q_scale[(w.q_start + i) * p.hq + w.h] : 1.f) * p.k_scale[w.g];
+        c *= f;
+        sc *= f;
       }
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n_tiles; ++j) {
@@ -658,7 +695,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (i >= 0 && i < Lq && p.lse != nullptr)
         p.lse[(w.q_start + i) * p.hq + w.h] =
-            (l > 0.f) ? m_ref * p.scale + log2f(l) * 0.69314718055994531f : -INFINITY;
+            (l > 0.f) ? m_ref * sc + log2f(l) * 0.69314718055994531f : -INFINITY;
       gt += n_tiles;
       if (n_tiles > 0) ++nq;
     }
@@ -681,17 +718,19 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restr
   }
 }
 
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
-  using C = AttnCfg<D>;
+  using C = AttnCfg<D, F8>;
   AttnMaps maps;
+  // es: bytes per value (2: bf16, 1: e4m3 q / k)
   auto make = [&](CUtensorMap* m, const void* base, int64_t tokens, int heads, uint32_t box0,
-                  CUtensorMapSwizzle sw) -> bool {
+                  CUtensorMapSwizzle sw, int es = 2) -> bool {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)heads, (uint64_t)tokens};
-    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)heads * D * 2};
+    const uint64_t strides[2] = {(uint64_t)D * es, (uint64_t)heads * D * es};
     const uint32_t box[3] = {box0, 1, (uint32_t)kBlockN};
-    CUresult r = encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                                   const_cast<void*>(base), dims, strides, box, sw);
+    CUresult r = encode_tensor_map(
+        m, es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+        const_cast<void*>(base), dims, strides, box, sw);
     if (r != CUDA_SUCCESS) {
       *drv_err = (int)r;
       return false;
@@ -699,8 +738,9 @@ cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
     return true;
   };
   const int64_t tq = a.total_q > 0 ? a.total_q : 1, tk = a.total_k > 0 ? a.total_k : 1;
-  if (!make(&maps.q, a.q, tq, a.hq, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make(&maps.k, a.k, tk, a.hkv, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  constexpr int qk_es = F8 ? 1 : 2;
+  if (!make(&maps.q, a.q, tq, a.hq, C::kQKCols, CU_TENSOR_MAP_SWIZZLE_128B, qk_es) ||
+      !make(&maps.k, a.k, tk, a.hkv, C::kQKCols, CU_TENSOR_MAP_SWIZZLE_128B, qk_es) ||
       !make(&maps.v, a.v, tk, a.hkv, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if constexpr (C::kTail != 0) {
@@ -730,6 +770,8 @@ cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
   p.pairs_max = (a.max_seqlen_q + 2 * kBlockM - 1) / (2 * kBlockM);
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
   const int64_t items = (int64_t)a.batch * p.pairs_max * a.hq;
   if (items == 0) return cudaSuccess;
   if (items > 0x7FFFFFFF || a.work_counter == nullptr) return cudaErrorInvalidConfiguration;
@@ -741,12 +783,12 @@ cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   // One persistent CTA per SM (the kernel's shared memory and TMEM allow one).
   const int grid = (int)(items < sms ? items : sms);
-  e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(a.work_counter, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D><<<grid, kAttnThreads, C::kSmemBytes, stream>>>(maps, p);
+  attn_fwd_kernel<D, F8><<<grid, kAttnThreads, C::kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -754,9 +796,10 @@ cudaError_t launch_d(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, int* drv_err, cudaStream_t stream) {
   switch (a.d) {
-    case 64: return launch_d<64>(a, drv_err, stream);
-    case 80: return launch_d<80>(a, drv_err, stream);
-    case 128: return launch_d<128>(a, drv_err, stream);
+    case 64: return a.fp8 ? cudaErrorInvalidValue : launch_d<64>(a, drv_err, stream);
+    case 80: return a.fp8 ? cudaErrorInvalidValue : launch_d<80>(a, drv_err, stream);
+    case 128: return a.fp8 ? launch_d<128, true>(a, drv_err, stream)
+                           : launch_d<128>(a, drv_err, stream);
     default: return cudaErrorInvalidValue;
   }
 }

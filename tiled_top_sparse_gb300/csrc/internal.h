@@ -39,10 +39,17 @@ struct AttnArgs {
   float* lse;
   uint32_t* dev_status;
   uint32_t* work_counter;  // device scratch word (the launch zeroes it on the stream)
+  bool fp8 = false;        // q, k are e4m3 codes with the scales below (head_dim 128)
+  const float* q_scale = nullptr;  // [total_q, hq]
+  const float* k_scale = nullptr;  // [hkv]
 };
 // Returns cudaSuccess or the first error; *drv_err receives a CUresult from tensor-map encoding.
 cudaError_t launch_attn_fwd(const AttnArgs& a, int* drv_err, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);
+// e4m3 block quantization of the prefill's q (per token and head) and k (per KV head).
+cudaError_t launch_quant_fp8_prefill(const void* q, int64_t total_q, int hq, const void* k,
+                                     int64_t total_k, int hkv, int d, void* q8, float* q_scale,
+                                     void* k8, float* k_scale, cudaStream_t stream);
 
 // ---- sparse attention
 struct SparseArgs {
