@@ -45,7 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNELS = {"vision": "attn_fwd_kernel<80>", "varlen": "attn_fwd_kernel<128>",
            "topk": "topk_select_kernel", "sparse": "sparse_attn_kernel"}
 KERNEL_SOURCES = {"vision": "attn_fwd.cu", "varlen": "attn_fwd.cu", "topk": "topk.cu",
-                  "sparse": "sparse_attn.cu", "vision_qkv_rope": "qkv_rope.cu"}
+                  "sparse": "sparse_attn.cu", "vision_qkv_rope": "qkv_rope.cu",
+                  "varlen_fp8": "attn_fwd.cu"}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -495,6 +496,58 @@ def qkv_rope_protocol(step, dev, peaks, flush):
             "protocol": "median of 20 single calls, CUDA events, L2 flushed before each"}
 
 
+def fp8_prefill_protocol(step, dev, peaks, flush):
+    """The varlen prefill workload (8 sequences, 32 / 8 heads, d 128, causal) through the
+    FP8 path, outside the step: the e4m3 quantization of q and k, then attention with e4m3
+    q / k in Q K^T. Each of 20 rounds flushes L2 (256 MB) before the quantization and
+    again before the attention, both timed with CUDA events on their stream; medians are
+    reported. The output of every round is checked against the first."""
+    t = step.tts
+    q, k, v, cq, ck = step.d_var
+    var = step.var
+    out = torch.empty(var.q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty(var.q.shape[:2], dtype=torch.float32, device=dev)
+    q8, qs, k8, ks = t.quantize_fp8_prefill(q, k)
+    s = torch.cuda.Stream(dev)
+    tq, ta, ref = [], [], None
+    with torch.cuda.stream(s):
+        for it in range(24):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            flush.zero_()
+            ev[0].record(s)
+            t.quantize_fp8_prefill(q, k, q8=q8, q_scale=qs, k8=k8, k_scale=ks)
+            ev[1].record(s)
+            flush.zero_()
+            ev[2].record(s)
+            t.attn_fwd_varlen_fp8(q8, qs, k8, ks, v, cq, ck, var.max_seqlen_q,
+                                  var.max_seqlen_k, True, var.scale, out=out, lse=lse,
+                                  workspace=step.ws, status=step.status)
+            ev[3].record(s)
+            ev[3].synchronize()
+            if it >= 4:
+                tq.append(ev[0].elapsed_time(ev[1]) * 1e3)
+                ta.append(ev[2].elapsed_time(ev[3]) * 1e3)
+            if ref is None:
+                ref = out.clone()
+    assert torch.equal(out, ref), "fp8 prefill: rounds disagree"
+    us_q, us_a = float(np.median(tq)), float(np.median(ta))
+    flops = var.flops()
+    tf = flops / (us_a * 1e-6) / 1e12
+    qbytes = (q.numel() + k.numel()) * 2 * 2 + (q.numel() + k.numel()) + qs.numel() * 4
+    del out, lse, q8, k8, ref
+    return {"workload": "varlen causal GQA prefill (the step's batch), e4m3 q / k in Q K^T, "
+                        "bf16 P V", "kernels": ["quant_rows_kernel", "head_amax_kernel",
+                                                "head_scale_kernel", "attn_fwd_kernel<128, true>"],
+            "us_quantize": us_q, "us_attention": us_a, "flops": flops, "tflops": tf,
+            "frac_bf16_peak": tf / peaks["bf16_tflops"],
+            "quantize_gbs": qbytes / (us_q * 1e-6) / 1e9,
+            "peak_source": "bf16_tflops (half of the MMA work, P V, stays bf16)",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                         "traffic": profiled_traffic("varlen_fp8")},
+            "protocol": "median of 20 rounds, CUDA events, L2 flushed before each call"}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(n_rows: int = 192, n_queries: int = 8):
     """Time the float64 oracle on bounded samples of each part.
@@ -685,6 +738,9 @@ def run_gpu(args, rank, world, local):
     if "topk" in parts and rank == 0:
         comp["topk"].update(topk_protocol(step, dev, peaks))
         comp["topk_long"] = topk_long_protocol(step, dev, peaks)
+    if "varlen" in parts and rank == 0:
+        comp["varlen_fp8"] = fp8_prefill_protocol(step, dev, peaks, flush)
+        tts.check_status(step.status, "bench fp8 prefill protocol")
     if "vision" in parts and rank == 0:
         comp["vision_qkv_rope"] = qkv_rope_protocol(step, dev, peaks, flush)
         tts.check_status(step.status, "bench qkv_rope protocol")

@@ -45,9 +45,10 @@ def codes(t):
     return t.view(torch.float8_e4m3fn).float().cpu().numpy()
 
 
-def test_quantization_bit_exact():
+@pytest.mark.parametrize("d", [128, 64, 132])   # 128: half-warp rows; others: warp rows
+def test_quantization_bit_exact(d):
     import tiled_top_sparse_gb300 as tts
-    inp = W.dense_inputs([300, 77], hq=6, hkv=3, d=128, seed=50)
+    inp = W.dense_inputs([300, 77], hq=6, hkv=3, d=d, seed=50)
     q, k = inp.q.clone(), inp.k.clone()
     g = torch.Generator().manual_seed(51)
     # rows over a wide range of magnitudes (subnormal codes included), an all-zero row,

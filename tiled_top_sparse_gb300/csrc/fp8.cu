@@ -41,8 +41,8 @@ __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16* p) {
 }
 
 // One warp per row of d values (d a multiple of 4): row maximum, its scale, the codes.
-// scale_of_row >= 0: the row's own scale is computed and written to row_scale;
-// otherwise the scale comes from the per-head maximum bits in head_amax[row % heads].
+// Without head_amax the row's own scale is computed and written to row_scale; with it
+// the scale comes from the per-head maximum bits in head_amax[row % heads].
 __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int d,
                                   uint8_t* __restrict__ codes, float* __restrict__ row_scale,
                                   const uint32_t* __restrict__ head_amax, int heads) {
@@ -69,6 +69,62 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t r
     for (int c = lane * 4; c < d; c += 128) {
       const float4 v = load_bf16x4(xr + c);
       *reinterpret_cast<uint32_t*>(codes + r * d + c) = e4m3x4(v.x / s, v.y / s, v.z / s, v.w / s);
+    }
+  }
+}
+
+// d = 128: half a warp per row (8 values, 16 bytes per lane), four rows per half-warp
+// loaded before any arithmetic, so a warp keeps 2 KB of loads in flight (the one-warp-
+// per-row loop above keeps 256 bytes). The same scales and codes as quant_rows_kernel.
+constexpr int kFastRows = 4;
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    f[2 * i] = __low2float(b);
+    f[2 * i + 1] = __high2float(b);
+  }
+}
+__global__ void quant_rows128_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                                     uint8_t* __restrict__ codes, float* __restrict__ row_scale,
+                                     const uint32_t* __restrict__ head_amax, int heads) {
+  const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t warp_id = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
+  // The loop bound is the warp's (both halves run every iteration, so the shuffles
+  // always see all 32 lanes); rows past the end are masked.
+  for (int64_t wb = warp_id * 2 * kFastRows; wb < rows; wb += nwarps * 2 * kFastRows) {
+    const int64_t rb = wb + half * kFastRows;
+    uint4 u[kFastRows];
+#pragma unroll
+    for (int j = 0; j < kFastRows; ++j) {
+      const int64_t r = rb + j;
+      u[j] = r < rows ? *reinterpret_cast<const uint4*>(x + r * 128 + hl * 8)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kFastRows; ++j) {
+      const int64_t r = rb + j;
+      float f[8];
+      bf16x8_to_f32(u[j], f);
+      float s;
+      if (head_amax == nullptr) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        s = amax > 0.f ? amax / 448.0f : 1.0f;
+        if (hl == 0 && r < rows) row_scale[r] = s;
+      } else {
+        const float amax = r < rows ? __uint_as_float(head_amax[r % heads]) : 0.f;
+        s = amax > 0.f ? amax / 448.0f : 1.0f;
+      }
+      if (r < rows)
+        *reinterpret_cast<uint2*>(codes + r * 128 + hl * 8) =
+            make_uint2(e4m3x4(f[0] / s, f[1] / s, f[2] / s, f[3] / s),
+                       e4m3x4(f[4] / s, f[5] / s, f[6] / s, f[7] / s));
     }
   }
 }
@@ -113,6 +169,25 @@ int row_blocks(int64_t rows) {
   if (b > 152 * 8) b = 152 * 8;
   return static_cast<int>(b < 1 ? 1 : b);
 }
+int row128_blocks(int64_t rows) {
+  const int64_t per_block = (kQuantThreads / 32) * 2 * kFastRows;  // rows per block and pass
+  int64_t b = (rows + per_block - 1) / per_block;
+  if (b > 152 * 8) b = 152 * 8;
+  return static_cast<int>(b < 1 ? 1 : b);
+}
+
+cudaError_t quant_rows(const void* x, int64_t rows, int d, void* codes, float* row_scale,
+                       const uint32_t* head_amax, int heads, cudaStream_t stream) {
+  if (d == 128)
+    quant_rows128_kernel<<<row128_blocks(rows), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, static_cast<uint8_t*>(codes), row_scale,
+        head_amax, heads);
+  else
+    quant_rows_kernel<<<row_blocks(rows), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, d, static_cast<uint8_t*>(codes), row_scale,
+        head_amax, heads);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -121,10 +196,7 @@ cudaError_t launch_quant_fp8_prefill(const void* q, int64_t total_q, int hq, con
                                      void* k8, float* k_scale, cudaStream_t stream) {
   const int64_t qrows = total_q * hq, krows = total_k * hkv;
   if (qrows > 0) {
-    quant_rows_kernel<<<row_blocks(qrows), kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(q), qrows, d, static_cast<uint8_t*>(q8), q_scale,
-        nullptr, 1);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = quant_rows(q, qrows, d, q8, q_scale, nullptr, 1, stream);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = cudaMemsetAsync(k_scale, 0, sizeof(float) * hkv, stream);
@@ -135,10 +207,7 @@ cudaError_t launch_quant_fp8_prefill(const void* q, int64_t total_q, int hq, con
         static_cast<const __nv_bfloat16*>(k), krows, d, hkv, amax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    quant_rows_kernel<<<row_blocks(krows), kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(k), krows, d, static_cast<uint8_t*>(k8), nullptr, amax,
-        hkv);
-    e = cudaGetLastError();
+    e = quant_rows(k, krows, d, k8, nullptr, amax, hkv, stream);
     if (e != cudaSuccess) return e;
   }
   head_scale_kernel<<<(hkv + 127) / 128, 128, 0, stream>>>(k_scale, hkv);
