@@ -25,6 +25,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -90,7 +91,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # The raw samples go to $TTS_CLOCKS_DIR when set (kept for inspection), else to a
+        # temporary directory; the JSON line carries their summary either way.
+        out_dir = os.environ.get("TTS_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
