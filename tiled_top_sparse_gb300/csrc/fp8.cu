@@ -155,6 +155,43 @@ __global__ void head_amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t ro
     if (s_amax[h] != 0u) atomicMax(&head_amax[h], s_amax[h]);
 }
 
+// d = 128: the same per-head maxima with half a warp per row and four rows per half-warp
+// in flight (the layout of quant_rows128_kernel).
+__global__ void head_amax128_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                                    int heads, uint32_t* __restrict__ head_amax) {
+  extern __shared__ uint32_t s_amax[];  // [heads]
+  for (int h = threadIdx.x; h < heads; h += blockDim.x) s_amax[h] = 0u;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t warp_id = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (int64_t wb = warp_id * 2 * kFastRows; wb < rows; wb += nwarps * 2 * kFastRows) {
+    const int64_t rb = wb + half * kFastRows;
+    uint4 u[kFastRows];
+#pragma unroll
+    for (int j = 0; j < kFastRows; ++j) {
+      const int64_t r = rb + j;
+      u[j] = r < rows ? *reinterpret_cast<const uint4*>(x + r * 128 + hl * 8)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kFastRows; ++j) {
+      float f[8];
+      bf16x8_to_f32(u[j], f);
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      const int64_t r = rb + j;
+      if (hl == 0 && r < rows) atomicMax(&s_amax[r % heads], __float_as_uint(amax));
+    }
+  }
+  __syncthreads();
+  for (int h = threadIdx.x; h < heads; h += blockDim.x)
+    if (s_amax[h] != 0u) atomicMax(&head_amax[h], s_amax[h]);
+}
+
 // The per-head maximum bits become the per-head scales.
 __global__ void head_scale_kernel(float* k_scale, int heads) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
@@ -203,8 +240,12 @@ cudaError_t launch_quant_fp8_prefill(const void* q, int64_t total_q, int hq, con
   if (e != cudaSuccess) return e;
   uint32_t* amax = reinterpret_cast<uint32_t*>(k_scale);
   if (krows > 0) {
-    head_amax_kernel<<<row_blocks(krows), kQuantThreads, sizeof(uint32_t) * hkv, stream>>>(
-        static_cast<const __nv_bfloat16*>(k), krows, d, hkv, amax);
+    if (d == 128)
+      head_amax128_kernel<<<row128_blocks(krows), kQuantThreads, sizeof(uint32_t) * hkv,
+                            stream>>>(static_cast<const __nv_bfloat16*>(k), krows, hkv, amax);
+    else
+      head_amax_kernel<<<row_blocks(krows), kQuantThreads, sizeof(uint32_t) * hkv, stream>>>(
+          static_cast<const __nv_bfloat16*>(k), krows, d, hkv, amax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = quant_rows(k, krows, d, k8, nullptr, amax, hkv, stream);
