@@ -7,7 +7,8 @@
  * - Pointers named as device pointers must point to device memory of the
  *   current CUDA device; sizes and scalars are host values. The caller owns
  *   all memory. The library allocates nothing and keeps no state between
- *   calls except a cached driver entry point.
+ *   calls except a cached driver entry point and, per device, the number of
+ *   CTA pairs tts_qkv_rope can keep resident (queried on its first call).
  * - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
  *   entry point only enqueues work on that stream; none synchronises.
  * - Host-side argument errors return a non-OK status and enqueue nothing.
