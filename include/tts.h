@@ -7,8 +7,12 @@
  * - Pointers named as device pointers must point to device memory of the
  *   current CUDA device; sizes and scalars are host values. The caller owns
  *   all memory. The library allocates nothing and keeps no state between
- *   calls except a cached driver entry point and, per device, the number of
+ *   calls except cached driver entry points and, per device, the number of
  *   CTA pairs tts_qkv_rope can keep resident (queried on its first call).
+ *   One exception: tts_attn_fwd_varlen_f32_noalloc (end of this file) uses a
+ *   fixed TTS_NOALLOC_SCRATCH_BYTES array of device memory that the library
+ *   itself holds on every GPU that loads it, and caches that array's address
+ *   per device and context.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
  *   entry point only enqueues work on that stream; none synchronises.
  * - Host-side argument errors return a non-OK status and enqueue nothing.
@@ -384,13 +388,17 @@ tts_status tts_debug_wait_timeout(uint32_t* dev_status, void* stream);
  * calls no allocator. Everything else -- arguments, layouts, results, errors -- is
  * as for tts_attn_fwd_varlen with in_dtype = TTS_F32.
  *
- * - Inputs whose bf16 copies need more than TTS_NOALLOC_SCRATCH_BYTES, i.e.
- *   2 * (total_q * num_heads_q + 2 * total_k * num_heads_kv) * head_dim bytes
- *   (each part rounded up to 256), are rejected with TTS_ERR_WORKSPACE before any
- *   work is enqueued.
+ * - The call needs tts_attn_workspace_bytes(total_q, total_k, num_heads_q,
+ *   num_heads_kv, head_dim, TTS_F32) bytes of the array: 256 bytes for the work
+ *   counter, plus the bf16 copies, 2 * total_q * num_heads_q * head_dim bytes for q
+ *   and 2 * total_k * num_heads_kv * head_dim bytes each for k and v, every copy
+ *   rounded up to a multiple of 256. Inputs that need more than
+ *   TTS_NOALLOC_SCRATCH_BYTES are rejected with TTS_ERR_WORKSPACE before any work
+ *   is enqueued.
  * - The first call on a device looks up the array's device address on that device
- *   (which must be current) and caches it; make that first call before capturing
- *   a stream into a CUDA graph.
+ *   (which must be current) and caches it per context, so a new context (after a
+ *   device reset, say) looks it up again; make that first call before capturing a
+ *   stream into a CUDA graph.
  * - Every call on a device shares the one array, which keeps the last call's
  *   contents; nothing in it needs to start at zero, because each call overwrites
  *   every byte it reads. Calls that overlap on the GPU (e.g. on two streams at

@@ -453,6 +453,35 @@ def test_rope_cache_rows_are_powers_of_the_first():
     np.testing.assert_allclose(np.abs(z), 1.0, atol=1e-15)
 
 
+def test_rope_cache_frequencies_closed_form():
+    # The angle of position 1, pair j is base^(-2j/d): an exponent of -j/d or a base
+    # other than the stated one fails here (every angle is below pi, so atan2 recovers it).
+    for d, base in ((80, 10000.0), (64, 10000.0), (128, 500000.0)):
+        c = oracle.rope_cache(2, d, base)
+        j = np.arange(d // 2)
+        np.testing.assert_allclose(np.arctan2(c[1, :, 1], c[1, :, 0]), base ** (-2.0 * j / d),
+                                   rtol=1e-13, atol=0)
+        np.testing.assert_array_equal(c[0, :, 0], 1.0)
+        np.testing.assert_array_equal(c[0, :, 1], 0.0)
+
+
+def test_rope_cache_equals_qkv_rope_with_identity_projection():
+    # With W = I and x = e_j the projected q is e_j, and RoPE turns it into
+    # cos(angle) e_j + sin(angle) e_{j+d/2}: the cache and the fused step must agree.
+    d = 80
+    h = d // 2
+    eye = np.eye(3 * d, dtype=np.float32)
+    positions = [0, 1, 7, 1000, 8546, 32767]
+    cache = oracle.rope_cache(32768, d)
+    for pos in positions:
+        x = eye[:h]                                   # token j carries e_j in the q part
+        q, k, _ = oracle.qkv_rope(x, eye, None, np.full(h, pos), heads=1, d=d)
+        j = np.arange(h)
+        np.testing.assert_allclose(q[j, 0, j], cache[pos, :, 0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(q[j, 0, j + h], cache[pos, :, 1], rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(k, np.zeros_like(k))  # x has no k part
+
+
 # ---- FP8 (e4m3) rounding and block quantization ----------------------------------------
 
 def _e4m3_table():

@@ -37,6 +37,20 @@ def call_noalloc(L, inp, out, lse, status):
     return code
 
 
+def run_both(tts, L, inp, dev):
+    """The allocation-free call, then the workspace call, on the same inputs."""
+    out = torch.full(inp.q.shape, float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full(inp.q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    assert call_noalloc(L, inp, out, lse, st) == tts.TTS_OK
+    ref_o, ref_l = tts.attn_fwd_varlen(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev),
+                                       inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev),
+                                       inp.max_seqlen_q, inp.max_seqlen_k, inp.causal, inp.scale)
+    torch.cuda.synchronize()
+    tts.check_status(st)
+    return out, lse, ref_o, ref_l
+
+
 def test_noalloc_matches_workspace_entry_point_twice():
     import tiled_top_sparse_gb300 as tts
     L = tts.lib()
@@ -45,18 +59,33 @@ def test_noalloc_matches_workspace_entry_point_twice():
              W.dense_inputs([300, 77, 129], hq=4, hkv=2, d=128, causal=True,
                             dtype=torch.float32, seed=60)]
     for inp in cases:  # two calls in a row share the one scratch array
-        out = torch.full(inp.q.shape, float("nan"), dtype=torch.float32, device=dev)
-        lse = torch.full(inp.q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
-        st = torch.zeros(1, dtype=torch.int32, device=dev)
-        assert call_noalloc(L, inp, out, lse, st) == tts.TTS_OK
-        ref_o, ref_l = tts.attn_fwd_varlen(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev),
-                                           inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev),
-                                           inp.max_seqlen_q, inp.max_seqlen_k, inp.causal,
-                                           inp.scale)
-        torch.cuda.synchronize()
-        tts.check_status(st)
+        out, lse, ref_o, ref_l = run_both(tts, L, inp, dev)
+        # Same kernel on the same bf16-rounded inputs: the results must be bitwise equal,
+        # so stale scratch contents cannot hide inside a tolerance.
+        assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
         assert_close_attn(out.cpu().numpy(), ref_o.cpu().double().numpy(), "noalloc vs workspace")
         assert_lse_close(lse.cpu().numpy(), ref_l.cpu().double().numpy(), "noalloc lse")
+
+
+def test_noalloc_at_the_scratch_limit_and_one_step_over():
+    import tiled_top_sparse_gb300 as tts
+    L = tts.lib()
+    dev = torch.device("cuda")
+    # 256 (work counter) + 2 * 21846 * 64 (q copy) + 2 * (2 * 21844 * 64) (k, v copies),
+    # every part a multiple of 256: exactly the array's size.
+    tq, tk = 21846, 21844
+    assert 256 + 2 * tq * 64 + 2 * (2 * tk * 64) == SCRATCH_BYTES
+    assert tts.attn_workspace_bytes(tq, tk, 1, 1, 64, torch.float32) == SCRATCH_BYTES
+    inp = W.dense_inputs([tq], [tk], hq=1, hkv=1, d=64, causal=False, dtype=torch.float32,
+                         seed=62)
+    out, lse, ref_o, ref_l = run_both(tts, L, inp, dev)
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    # two more query rows need 256 bytes more than the array holds
+    over = W.dense_inputs([tq + 2], [tk], hq=1, hkv=1, d=64, causal=False, dtype=torch.float32,
+                          seed=63)
+    assert tts.attn_workspace_bytes(tq + 2, tk, 1, 1, 64, torch.float32) == SCRATCH_BYTES + 256
+    o2 = torch.zeros(over.q.shape, dtype=torch.float32, device=dev)
+    assert call_noalloc(L, over, o2, None, None) == tts.TTS_ERR_WORKSPACE
 
 
 def test_noalloc_rejects_inputs_larger_than_scratch():

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tts.h"
@@ -25,23 +26,60 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+// Per device: the context the address was looked up in, and the address. A device
+// reset (or a released and re-created primary context) loads the module again, and
+// the array may then sit at another address; a new context triggers a new lookup.
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;  // the driver's unique context id (never reused)
+  void* ptr = nullptr;
+};
+ScratchSlot g_slot[kMaxDevices];
 
-// Device address of the scratch array on the current device; looked up once per
-// device (with that device current) and cached.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+void* driver_fn(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return f;
+}
+
+// Unique id of the calling thread's current context; 0 when none is current.
+CUresult current_ctx_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent"));
+  static const CtxGetIdFn get_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId"));
+  *id = 0;
+  if (get == nullptr || get_id == nullptr) return CUDA_ERROR_NOT_SUPPORTED;
+  CUcontext ctx = nullptr;
+  CUresult r = get(&ctx);
+  if (r != CUDA_SUCCESS || ctx == nullptr) return r;
+  return get_id(ctx, id);
+}
+
+// Device address of the scratch array in the current context of the current device;
+// looked up once per (device, context), with that device current, and cached.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long id = 0;
+  if (current_ctx_id(&id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  ScratchSlot& s = g_slot[dev];
+  if (id == 0 || s.ptr == nullptr || s.ctx_id != id) {
+    // The lookup also makes the device's primary context current when no context is.
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    if (current_ctx_id(&id) != CUDA_SUCCESS || id == 0) return cudaErrorDeviceUninitialized;
+    s.ctx_id = id;
+    s.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = s.ptr;
   return cudaSuccess;
 }
 

@@ -34,6 +34,7 @@
 //               the accumulator is handed back to the leader's MMA warp by local /
 //               remote arrives.
 // Pair tiles go to pairs round-robin; every wait is bounded.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -465,8 +466,13 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
 // Co-resident CTA pairs of qkv_rope_kernel<D> on the current device (cached per device).
 template <int D>
 int max_pairs(int dev, const cudaLaunchConfig_t& cfg) {
-  static int cache[64] = {0};
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  // Host threads may make their first calls at the same time: every thread that finds
+  // the slot empty computes the same value, and the slot is read and written atomically.
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, qkv_rope_kernel<D>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
@@ -474,7 +480,7 @@ int max_pairs(int dev, const cudaLaunchConfig_t& cfg) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     n = sms / 2 > 0 ? sms / 2 : 1;
   }
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
