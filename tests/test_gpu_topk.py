@@ -107,3 +107,39 @@ def test_output_canaries_untouched(tts):
     assert bool((buf[:4096] == -12345).all()) and bool((buf[-4096:] == -12345).all())
     ref, _ = oracle_idx(inp)
     assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+def test_bucket_limit_and_mixed_values(tts):
+    # Windows of up to 4096 values are ranked inside value buckets unless one bucket holds
+    # more than 128 values, when the whole window is radix-sorted instead; both must give
+    # the oracle's indices. Rows: 128 and 129 copies of one value among distinct ones
+    # (just inside / just past the limit), infinities and signed zeros among normals,
+    # one outlier that stretches the bucket range, all values negative, plain fp32
+    # values (not on the bf16 grid), and a 4096-value window.
+    g = torch.Generator().manual_seed(11)
+    rows = []
+    for copies in (128, 129):
+        x = torch.randn(3000, generator=g)
+        x[torch.randperm(3000, generator=g)[:copies]] = 4.5  # a value no normal draw shares a bucket with
+        rows.append(x)
+    x = torch.randn(3000, generator=g)
+    x[[3, 50, 900]] = float("inf")
+    x[[4, 51]] = float("-inf")
+    x[[5, 6, 7]] = 0.0
+    x[[8, 9]] = -0.0
+    rows.append(x)
+    x = torch.randn(3000, generator=g)
+    x[17] = 3e38
+    rows.append(x)
+    rows.append(-torch.randn(3000, generator=g).abs())
+    rows.append(torch.randn(3000, generator=g) * 1e-3 + 7.0)
+    logits = torch.stack(rows)
+    n = logits.shape[0]
+    inp = W.TopkInputs(logits, torch.zeros(n, dtype=torch.int32),
+                       torch.full((n,), 3000, dtype=torch.int32), 2048)
+    ref, _ = oracle_idx(inp)
+    assert np.array_equal(run(tts, inp).cpu().numpy(), ref)
+    full = W.TopkInputs(torch.randn(2, 4096, generator=g), torch.zeros(2, dtype=torch.int32),
+                        torch.full((2,), 4096, dtype=torch.int32), 4000)
+    ref, _ = oracle_idx(full)
+    assert np.array_equal(run(tts, full).cpu().numpy(), ref)

@@ -5,10 +5,14 @@
 // the k window positions with the largest values, ordered by value descending
 // and, among equal values, by ascending position.
 //
-// Windows of up to 4096 values (the indexer's rows are 2590 long) are ranked by a
-// stable LSD radix sort of the whole window on the inverted key (4 passes of 8 bits;
-// stability keeps equal values in ascending position), and the first k positions are
-// the answer. Longer windows take the select-then-sort path:
+// Windows of up to 4096 values (the indexer's rows are 2590 long) take the bucket-rank
+// path: a counting pass places value buckets (a linear map of each sign half's keys
+// onto 2048 buckets) at their final offsets, and each selectable element is ranked
+// inside its bucket by comparing unique (key, position) composites. A window whose
+// values pile up on few keys (a bucket of more than 128 values) takes a stable LSD
+// radix sort of the whole window on the inverted key instead (passes of 8 bits;
+// stability keeps equal values in ascending position). Both give the same result.
+// Longer windows take the select-then-sort path:
 //  1. map each float of the window to an order-preserving 32-bit key
 //     (-0 folded onto +0, so equal floats get equal keys);
 //  2. MSB-first radix select over 4 x 8-bit digits finds the key T of rank k
@@ -19,6 +23,7 @@
 //  4. sort the selected (key, position) pairs as one 64-bit composite
 //     (key << 32 | ~position) descending with a bitonic network. Composites are
 //     unique, so the result is fully determined by the input.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -196,6 +201,194 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
     out[j] = (j < n) ? (from_regs ? j : (int32_t)pos_buf[in * kSortMax + j]) : -1;
 }
 
+// Bucket-rank path for windows of up to kSortMax values.
+//
+// Every value gets the sort key skey = ~ordered_key (ascending skey = descending value,
+// -0 folded onto +0). The keys of each sign half (skey < 2^31: values >= +0; skey >= 2^31:
+// negative values) are mapped linearly onto kHalfBuckets buckets between the half's
+// smallest and largest key, so bucket order is key order, and a counting pass places
+// every bucket at its final offset. Inside a bucket the elements are ranked by the
+// unique composite (key offset inside the bucket << 12 | position), which orders
+// exactly as (value descending, position ascending); a bucket spans at most 2^19 key
+// codes (a half's span is below 2^31, divided into 2^12 buckets) and positions need
+// 12 bits, so the composite fits 31 bits. The rank of an element is the number of
+// smaller composites in its bucket, found by comparing against every member: cheap
+// while buckets hold a handful of values, which is the case unless the window's values
+// pile up on a few keys. Returns false, having written nothing, when some bucket holds
+// more than kMaxBucket values; the caller then takes the radix path, which gives the
+// same result. Buckets that start at or beyond k are never ranked: none of their
+// values is selected.
+constexpr int kHalfBits = 11;
+constexpr int kHalfBuckets = 1 << kHalfBits;
+constexpr int kBuckets = 2 * kHalfBuckets;
+constexpr uint32_t kMaxBucket = 128;
+static_assert(kBuckets == 8 * kTopkThreads, "the scan gives every thread one uint4 of counters");
+static_assert(kSortMax <= 4096, "positions must fit the composite's 12 bits");
+// Shared memory: bucket starts (16-bit counters, two to a word), insertion cursors,
+// the bucketed composites with their bucket ids, and the staged output.
+constexpr size_t kBucketSmem = 2 * (kBuckets / 2) * 4 + kSortMax * (4 + 2 + 4);
+
+__device__ __forceinline__ uint32_t half16(uint32_t word, uint32_t b) {
+  return (word >> ((b & 1u) * 16u)) & 0xFFFFu;
+}
+
+__device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n, int k,
+                                            int32_t* __restrict__ out, uint8_t* smem) {
+  uint32_t* const start = reinterpret_cast<uint32_t*>(smem);                  // [kBuckets/2]
+  uint32_t* const cur = reinterpret_cast<uint32_t*>(smem + 2 * kBuckets);     // [kBuckets/2]
+  uint32_t* const comp = reinterpret_cast<uint32_t*>(smem + 4 * kBuckets);    // [kSortMax]
+  uint16_t* const bid =
+      reinterpret_cast<uint16_t*>(smem + 4 * kBuckets + 4 * kSortMax);        // [kSortMax]
+  int32_t* const staged =
+      reinterpret_cast<int32_t*>(smem + 4 * kBuckets + 6 * kSortMax);         // [kSortMax]
+  __shared__ uint32_t s_rng[4];  // min / max skey of the non-negative half, then the negative
+  __shared__ uint32_t s_maxc, s_ranked;
+  __shared__ uint32_t s_wsum[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 4) s_rng[tid] = (tid & 1) ? 0u : 0xFFFFFFFFu;
+  if (tid == 0) {
+    s_maxc = 0u;
+    s_ranked = static_cast<uint32_t>(n);
+  }
+  reinterpret_cast<uint4*>(start)[tid] = make_uint4(0u, 0u, 0u, 0u);
+  // Element st of thread tid is window position st * kTopkThreads + tid (coalesced).
+  uint32_t sk[kSortPerThread];
+  uint32_t pmin = 0xFFFFFFFFu, pmax = 0u, nmin = 0xFFFFFFFFu, nmax = 0u;
+#pragma unroll
+  for (int st = 0; st < kSortPerThread; ++st) {
+    const int i = st * kTopkThreads + tid;
+    sk[st] = 0u;
+    if (i < n) {
+      uint32_t u = __float_as_uint(__ldg(src + i));
+      if ((u & 0x7FFFFFFFu) == 0) u = 0;
+      const uint32_t s = (u & 0x80000000u) ? u : ~(u | 0x80000000u);  // ~ordered_key
+      sk[st] = s;
+      if (s < 0x80000000u) {
+        pmin = min(pmin, s);
+        pmax = max(pmax, s);
+      } else {
+        nmin = min(nmin, s);
+        nmax = max(nmax, s);
+      }
+    }
+  }
+  pmin = __reduce_min_sync(0xFFFFFFFFu, pmin);
+  pmax = __reduce_max_sync(0xFFFFFFFFu, pmax);
+  nmin = __reduce_min_sync(0xFFFFFFFFu, nmin);
+  nmax = __reduce_max_sync(0xFFFFFFFFu, nmax);
+  __syncthreads();
+  if (lane == 0) {
+    atomicMin(&s_rng[0], pmin);
+    atomicMax(&s_rng[1], pmax);
+    atomicMin(&s_rng[2], nmin);
+    atomicMax(&s_rng[3], nmax);
+  }
+  __syncthreads();
+  // Per half: its smallest key and the shift that maps its span onto kHalfBuckets buckets.
+  // A half's span is below 2^31, so the shift is at most 20 and the composite (offset
+  // inside the bucket << 12 | position) fits 32 bits.
+  const uint32_t base0 = s_rng[0], base1 = s_rng[2];
+  const uint32_t span0 = s_rng[1] - base0, span1 = s_rng[3] - base1;  // garbage if empty
+  const int sh0 = max(0, (32 - __clz(span0)) - kHalfBits);
+  const int sh1 = max(0, (32 - __clz(span1)) - kHalfBits);
+  uint32_t bkt[kSortPerThread];
+#pragma unroll
+  for (int st = 0; st < kSortPerThread; ++st) {
+    const int i = st * kTopkThreads + tid;
+    bkt[st] = 0xFFFFFFFFu;
+    if (i < n) {
+      const uint32_t s = sk[st];
+      const bool neg = s >= 0x80000000u;
+      const uint32_t off = s - (neg ? base1 : base0);
+      const int sh = neg ? sh1 : sh0;
+      bkt[st] = (neg ? kHalfBuckets : 0) + (off >> sh);
+      sk[st] = ((off & ((1u << sh) - 1u)) << 12) | static_cast<uint32_t>(i);  // composite
+      atomicAdd(&start[bkt[st] >> 1], 1u << ((bkt[st] & 1u) * 16u));
+    }
+  }
+  __syncthreads();
+  // Exclusive prefix over the buckets in ascending order: thread tid owns buckets
+  // [8 tid, 8 tid + 8), one uint4 of counters. Counts and starts stay below 2^16. The
+  // thread whose bucket holds output place k - 1 records where that bucket ends: every
+  // slot before it is ranked, nothing after it is selected.
+  {
+    const uint4 c = reinterpret_cast<uint4*>(start)[tid];
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t tot = 0u, mx = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = w[j] & 0xFFFFu, hi = w[j] >> 16;
+      tot += lo + hi;
+      mx = max(mx, max(lo, hi));
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    uint32_t x = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_wsum[warp] = x;
+    if (lane == 0) atomicMax(&s_maxc, mx);
+    __syncthreads();
+    uint32_t run = x - tot;
+    const uint4* ws4 = reinterpret_cast<const uint4*>(s_wsum);
+#pragma unroll
+    for (int q = 0; q < kWarps / 4; ++q) {
+      const uint4 v = ws4[q];
+      run += (4 * q + 0 < warp ? v.x : 0u) + (4 * q + 1 < warp ? v.y : 0u) +
+             (4 * q + 2 < warp ? v.z : 0u) + (4 * q + 3 < warp ? v.w : 0u);
+    }
+    uint32_t o[4];
+    const uint32_t kk = static_cast<uint32_t>(k);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = w[j] & 0xFFFFu, hi = w[j] >> 16;
+      o[j] = run | ((run + lo) << 16);
+      if (run < kk && kk <= run + lo) s_ranked = run + lo;
+      if (run + lo < kk && kk <= run + lo + hi) s_ranked = run + lo + hi;
+      run += lo + hi;
+    }
+    const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(start)[tid] = ov;
+    reinterpret_cast<uint4*>(cur)[tid] = ov;
+  }
+  __syncthreads();
+  if (s_maxc > kMaxBucket) return false;  // uniform: every thread reads the same word
+  const uint32_t ranked = s_ranked;        // slots [0, ranked) hold the selectable buckets
+  // Scatter the composites of buckets that start before k (and their bucket ids).
+#pragma unroll
+  for (int st = 0; st < kSortPerThread; ++st) {
+    const uint32_t b = bkt[st];
+    if (b != 0xFFFFFFFFu && half16(start[b >> 1], b) < static_cast<uint32_t>(k)) {
+      const uint32_t old = atomicAdd(&cur[b >> 1], 1u << ((b & 1u) * 16u));
+      const uint32_t slot = half16(old, b);
+      comp[slot] = sk[st];
+      bid[slot] = static_cast<uint16_t>(b);
+    }
+  }
+  __syncthreads();
+  // Rank in bucket order: thread tid takes slots tid, tid + 512, ...; neighbouring lanes
+  // hold neighbouring slots, mostly of the same bucket, so their loads of the bucket's
+  // members coincide. The rank of a slot is the number of smaller composites in its
+  // bucket; its place is the bucket's start plus that rank.
+  for (uint32_t j = tid; j < ranked; j += kTopkThreads) {
+    const uint32_t me = comp[j];
+    const uint32_t b = bid[j];
+    const uint32_t s0 = half16(start[b >> 1], b);
+    const uint32_t s1 = (b + 1 < kBuckets) ? half16(start[(b + 1) >> 1], b + 1)
+                                           : static_cast<uint32_t>(n);
+    uint32_t rank = 0;
+    for (uint32_t m = s0; m < s1; ++m) rank += comp[m] < me ? 1u : 0u;
+    const uint32_t dst = s0 + rank;
+    if (dst < static_cast<uint32_t>(k)) staged[dst] = static_cast<int32_t>(me & 0xFFFu);
+  }
+  __syncthreads();
+  const int take = n < k ? n : k;
+  for (int j = tid; j < k; j += kTopkThreads) out[j] = (j < take) ? staged[j] : -1;
+  return true;
+}
+
 // Three CTAs per SM (<= 40 registers a thread): 456 resident rows on 152 SMs.
 __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
     const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
@@ -221,7 +414,10 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
   const int n = static_cast<int>(len);
   const float* src = logits + r * row_stride + st;
   if (n <= kSortMax) {
-    radix_topk(src, n, k, out, smem);
+    if (!bucket_topk(src, n, k, out, smem)) {
+      __syncthreads();  // the radix path reuses the shared memory
+      radix_topk(src, n, k, out, smem);
+    }
     return;
   }
   for (int j = tid; j < n; j += kTopkThreads) keys[j] = ordered_key(__ldg(src + j));
@@ -336,7 +532,8 @@ size_t topk_smem_bytes(int64_t row_stride, int k) {
   int sort_n = 2;
   while (sort_n < cap) sort_n <<= 1;
   const size_t sel = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
-  return sel < kRadixSmem ? kRadixSmem : sel;
+  const size_t small = kRadixSmem > kBucketSmem ? kRadixSmem : kBucketSmem;
+  return sel < small ? small : sel;
 }
 
 cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t rows,
@@ -347,12 +544,34 @@ cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t 
   while (sort_n < cap) sort_n <<= 1;
   size_t smem = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
   if (smem < kRadixSmem) smem = kRadixSmem;
-  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem < kBucketSmem) smem = kBucketSmem;
+  // The shared-memory limit is a per-device attribute of the kernel; raise it only when
+  // a call needs more than a previous call on this device set (races only repeat it).
+  static std::atomic<int> configured[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_relaxed) < (int)smem) {
+    e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev].store((int)smem, std::memory_order_relaxed);
+  }
   topk_select_kernel<<<rows, kTopkThreads, smem, stream>>>(logits, row_stride, row_starts,
                                                             row_lens, k, sort_n, idx, dev_status);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaErrorInvalidValue) {
+    // A new context (after a device reset, say) starts from the default limit: set it
+    // and launch once more (the refused launch ran nothing).
+    e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_select_kernel<<<rows, kTopkThreads, smem, stream>>>(logits, row_stride, row_starts,
+                                                              row_lens, k, sort_n, idx,
+                                                              dev_status);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace tts
