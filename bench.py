@@ -12,6 +12,12 @@ Prints one JSON line (rank 0). `value` = attention TFLOP/s of the whole step
 (dense + sparse FLOPs / step time); per-part figures are under `components`.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--shard [--gather]]
+
+Under torchrun with N ranks the default runs one whole step per GPU (weak scaling);
+--shard splits one step's units over the ranks instead (strong scaling: dense attention
+by (sequence, KV-head group), top-k by rows, sparse attention by queries; no exchange
+while computing, and with --gather one all-gather of the results at the end).
 
 `--impl reference` times the float64 CPU oracle (the only reference there is:
 the pages ship no code) on bounded samples of the same workload.
@@ -176,15 +182,23 @@ def max_over_ranks(x: float, world: int) -> float:
 class Step:
     """Device-resident inputs/outputs of one hot-path step and the four calls."""
 
-    def __init__(self, dev, small=False):
+    def __init__(self, dev, small=False, shard=None):
+        """shard = (rank, world): keep only this rank's units of the step (dense attention
+        by (sequence, KV-head group), top-k by rows, sparse attention by queries), packed
+        once here, outside any timed region. None: the whole step."""
         import tiled_top_sparse_gb300 as tts
+        from tiled_top_sparse_gb300 import shard as S
         self.tts = tts
         self.dev = dev
+        self.sharded = shard is not None
         self.vis = W.vision()
         # small: a profiling-sized varlen batch (still larger than L2 in total)
         self.var = W.varlen(lengths=[4096, 3000, 2000, 1000]) if small else W.varlen()
         self.tk = W.topk_inputs()
         self.sp = W.sparse_inputs()
+        # the whole step's work (every rank's units together)
+        self.flops_total = {"vision": self.vis.flops(), "varlen": self.var.flops(),
+                            "sparse": self.sp.flops()}
         g = lambda t: t.to(dev)  # noqa: E731
         self.d_vis = [g(self.vis.q), g(self.vis.k), g(self.vis.v), g(self.vis.cu_seqlens_q),
                       g(self.vis.cu_seqlens_k)]
@@ -192,31 +206,58 @@ class Step:
                       g(self.var.cu_seqlens_k)]
         self.d_tk = [g(self.tk.logits), g(self.tk.row_starts), g(self.tk.row_lens)]
         self.d_sp = [g(self.sp.q), g(self.sp.kv_cache), g(self.sp.page_table), g(self.sp.idx)]
-        f32 = dict(dtype=torch.float32, device=dev)
-        self.o_vis = torch.empty(self.vis.q.shape, **f32)
-        self.l_vis = torch.empty(self.vis.q.shape[:2], **f32)
-        self.o_var = torch.empty(self.var.q.shape, **f32)
-        self.l_var = torch.empty(self.var.q.shape[:2], **f32)
-        self.o_idx = torch.empty((self.tk.logits.shape[0], self.tk.k), dtype=torch.int32,
-                                 device=dev)
-        self.o_sp = torch.empty((self.sp.q.shape[0], self.sp.q.shape[1], self.sp.dv), **f32)
-        self.l_sp = torch.empty(self.sp.q.shape[:2], **f32)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        # attention workspace (work-item counter), shared by the two stream-ordered calls
-        ws = max(tts.attn_workspace_bytes(self.vis.q.shape[0], self.vis.k.shape[0],
-                                          self.vis.q.shape[1], self.vis.k.shape[1],
-                                          self.vis.q.shape[2], torch.bfloat16),
-                 tts.attn_workspace_bytes(self.var.q.shape[0], self.var.k.shape[0],
-                                          self.var.q.shape[1], self.var.k.shape[1],
-                                          self.var.q.shape[2], torch.bfloat16))
-        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
-        # sparse workspace: partial results of the split last wave
-        self.ws_sp = torch.empty(max(16, tts.sparse_workspace_bytes(self.sp.q.shape[0])),
-                                 dtype=torch.uint8, device=dev)
-        self.flops = {"vision": self.vis.flops(), "varlen": self.var.flops(),
-                      "sparse": self.sp.flops()}
+        self.mq = {"vision": (self.vis.max_seqlen_q, self.vis.max_seqlen_k),
+                   "varlen": (self.var.max_seqlen_q, self.var.max_seqlen_k)}
+        self.flops = dict(self.flops_total)
         self.topk_bytes = self.tk.bytes()
         self.gathered = self.sp.gathered_bytes()
+        self.n_rows = self.tk.logits.shape[0]
+        self.plan = None
+        if shard is not None:
+            rank, world = shard
+            self.plan = {}
+            for name, inp, d in (("vision", self.vis, self.d_vis), ("varlen", self.var,
+                                                                   self.d_var)):
+                hq, hkv = inp.q.shape[1], inp.k.shape[1]
+                owned, load = S.plan_dense(inp.lengths_q, inp.lengths_k, hq, hkv, inp.causal,
+                                           world)
+                sh = S.pack_dense(*d, owned[rank], hq, hkv)
+                d[:] = [sh.q, sh.k, sh.v, sh.cu_q, sh.cu_k]
+                self.mq[name] = (sh.max_q, sh.max_k)
+                self.flops[name] = self.flops_total[name] * load[rank] / max(1, sum(load))
+                self.plan[name] = {"units": len(owned[rank]), "heads_per_call": sh.hq,
+                                   "load_max_over_mean": max(load) * world / max(1, sum(load))}
+            r0, r1 = S.split_range(self.n_rows, world, rank)
+            self.d_tk = [t[r0:r1].contiguous() for t in self.d_tk]
+            self.topk_bytes = self.tk.bytes() * (r1 - r0) / max(1, self.n_rows)
+            self.n_rows = r1 - r0
+            n0, n1 = S.split_range(self.sp.q.shape[0], world, rank)
+            nq = self.sp.q.shape[0]
+            self.d_sp[0] = self.d_sp[0][n0:n1].contiguous()
+            self.d_sp[3] = self.d_sp[3][n0:n1].contiguous()
+            self.flops["sparse"] = self.flops_total["sparse"] * (n1 - n0) / nq
+            self.gathered = self.sp.gathered_bytes() * (n1 - n0) / nq
+            self.plan["topk"] = {"rows": [r0, r1]}
+            self.plan["sparse"] = {"queries": [n0, n1]}
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.o_vis = torch.empty(self.d_vis[0].shape, **f32)
+        self.l_vis = torch.empty(self.d_vis[0].shape[:2], **f32)
+        self.o_var = torch.empty(self.d_var[0].shape, **f32)
+        self.l_var = torch.empty(self.d_var[0].shape[:2], **f32)
+        self.o_idx = torch.empty((self.d_tk[0].shape[0], self.tk.k), dtype=torch.int32,
+                                 device=dev)
+        nq_here = self.d_sp[0].shape[0]
+        self.o_sp = torch.empty((nq_here, self.sp.q.shape[1], self.sp.dv), **f32)
+        self.l_sp = torch.empty((nq_here, self.sp.q.shape[1]), **f32)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # attention workspace (work-item counter), shared by the two stream-ordered calls
+        ws = max(tts.attn_workspace_bytes(d[0].shape[0], d[1].shape[0], d[0].shape[1],
+                                          d[1].shape[1], d[0].shape[2], torch.bfloat16)
+                 for d in (self.d_vis, self.d_var))
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # sparse workspace: partial results of the split last wave
+        self.ws_sp = torch.empty(max(16, tts.sparse_workspace_bytes(nq_here)),
+                                 dtype=torch.uint8, device=dev)
 
     def inputs(self):
         return self.d_vis[:3] + self.d_var[:3] + self.d_tk[:1] + self.d_sp[:2] + self.d_sp[3:]
@@ -228,14 +269,14 @@ class Step:
         t = self.tts
         if name == "vision":
             q, k, v, cq, ck = self.d_vis
-            t.attn_fwd_varlen(q, k, v, cq, ck, self.vis.max_seqlen_q, self.vis.max_seqlen_k,
-                              False, self.vis.scale, out=self.o_vis, lse=self.l_vis,
-                              workspace=self.ws, status=self.status)
+            t.attn_fwd_varlen(q, k, v, cq, ck, *self.mq["vision"], False, self.vis.scale,
+                              out=self.o_vis, lse=self.l_vis, workspace=self.ws,
+                              status=self.status)
         elif name == "varlen":
             q, k, v, cq, ck = self.d_var
-            t.attn_fwd_varlen(q, k, v, cq, ck, self.var.max_seqlen_q, self.var.max_seqlen_k,
-                              True, self.var.scale, out=self.o_var, lse=self.l_var,
-                              workspace=self.ws, status=self.status)
+            t.attn_fwd_varlen(q, k, v, cq, ck, *self.mq["varlen"], True, self.var.scale,
+                              out=self.o_var, lse=self.l_var, workspace=self.ws,
+                              status=self.status)
         elif name == "topk":
             lg, rs, rl = self.d_tk
             t.topk_select(lg, rs, rl, self.tk.k, idx=self.o_idx, status=self.status)
@@ -262,7 +303,10 @@ class Step:
         if "sparse" in parts:
             units.append(("sparse", list(self.d_sp), [self.o_sp, self.l_sp],
                           lambda: self.part("sparse")))
-        if "varlen" in parts:
+        if "varlen" in parts and self.sharded:
+            units.append(("varlen", list(self.d_var), [self.o_var, self.l_var],
+                          lambda: self.part("varlen")))
+        elif "varlen" in parts:
             q, k, v, cq, ck = self.d_var
             cu = self.var.cu_seqlens_q.tolist()
             assert cu == self.var.cu_seqlens_k.tolist()
@@ -672,16 +716,38 @@ def run_gpu(args, rank, world, local):
     torch.cuda.set_device(dev)
     import tiled_top_sparse_gb300 as tts
     tts.lib()
-    step = Step(dev, small=args.small)
+    step = Step(dev, small=args.small, shard=(rank, world) if args.shard else None)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
     parts = tuple(p for p in Step.PARTS if p in args.parts.split(","))
+
+    gather = None
+    if args.shard and args.gather and world > 1:
+        # The one collective of a sharded step: every rank's results to every rank (raw
+        # bytes, padded to the largest share), after its calls, inside the step's events.
+        import torch.distributed as dist
+        outs = [o for o in step.outputs()]
+        nbytes = sum(o.numel() * o.element_size() for o in outs)
+        mx = torch.tensor([nbytes], dtype=torch.int64, device=dev)
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        send = torch.zeros(int(mx.item()), dtype=torch.uint8, device=dev)
+        recv = torch.empty(world * send.numel(), dtype=torch.uint8, device=dev)
+
+        def gather():
+            off = 0
+            for o in outs:
+                b = o.numel() * o.element_size()
+                send[off:off + b].copy_(o.reshape(-1).view(torch.uint8))
+                off += b
+            dist.all_gather_into_tensor(recv, send)
 
     def one_step(ev=None):
         for i, p in enumerate(parts):
             if ev is not None:
                 ev[i].record(stream)
             step.part(p)
+        if gather is not None:
+            gather()
         if ev is not None:
             ev[len(parts)].record(stream)
 
@@ -715,7 +781,10 @@ def run_gpu(args, rank, world, local):
     ms_step_local = float(np.mean(step_ms))
     ms_step = max_over_ranks(ms_step_local, world)
     attn_flops = sum(step.flops[p] for p in parts if p in step.flops)
-    value = world * attn_flops / (ms_step * 1e-3) / 1e12
+    # replicas: every rank runs the whole step; sharded: the ranks share one step
+    job_flops = (sum(step.flops_total[p] for p in parts if p in step.flops_total)
+                 if args.shard else world * attn_flops)
+    value = job_flops / (ms_step * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
     timed_s = t_wall1 - t_wall0
@@ -730,7 +799,7 @@ def run_gpu(args, rank, world, local):
             c.update({"tflops": tf, "frac_bf16_peak": tf / tensor_peak})
         elif p == "topk":
             gbs = step.topk_bytes / (ms * 1e-3) / 1e9
-            c.update({"rows_per_s": step.tk.logits.shape[0] / (ms * 1e-3), "gbs": gbs,
+            c.update({"rows_per_s": step.n_rows / (ms * 1e-3), "gbs": gbs,
                       "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": step.topk_bytes})
         else:
             gbs = step.gathered / (ms * 1e-3) / 1e9
@@ -739,16 +808,17 @@ def run_gpu(args, rank, world, local):
                       "gathered_bytes": step.gathered, "tflops": tf,
                       "frac_bf16_peak": tf / tensor_peak})
         comp[p] = c
-    if "topk" in parts and rank == 0:
+    extra = not args.shard  # the single-GPU protocols below measure whole workloads
+    if "topk" in parts and rank == 0 and extra:
         comp["topk"].update(topk_protocol(step, dev, peaks))
         comp["topk_long"] = topk_long_protocol(step, dev, peaks)
-    if "varlen" in parts and rank == 0:
+    if "varlen" in parts and rank == 0 and extra:
         comp["varlen_fp8"] = fp8_prefill_protocol(step, dev, peaks, flush)
         tts.check_status(step.status, "bench fp8 prefill protocol")
-    if "vision" in parts and rank == 0:
+    if "vision" in parts and rank == 0 and extra:
         comp["vision_qkv_rope"] = qkv_rope_protocol(step, dev, peaks, flush)
         tts.check_status(step.status, "bench qkv_rope protocol")
-    if "sparse" in parts and rank == 0:
+    if "sparse" in parts and rank == 0 and extra:
         comp["sparse_decode"] = decode_protocol(step, dev, peaks)
         tts.check_status(step.status, "bench decode protocol")
         tts.check_status(step.status, "bench top-k protocol")
@@ -807,7 +877,7 @@ def run_gpu(args, rank, world, local):
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
         ms_e2e = max_over_ranks(float(np.median(times[1:])), world)
-        e2e = {"value": world * attn_flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": int(sum(x.numel() * x.element_size()
                                              for u in units for x in u[1])),
@@ -827,10 +897,14 @@ def run_gpu(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1
-                   else "single GPU", "lengths_varlen": step.var.lengths_q,
+        "higher_is_better": True, "scaling": "strong" if args.shard else "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD,
+                   "parallelism": (f"one step sharded over {world} GPUs: dense attention by "
+                                   "(sequence, KV-head group), top-k by rows, sparse attention "
+                                   "by queries" + (", results all-gathered" if gather else ""))
+                   if args.shard else (f"replicas x{world}" if world > 1 else "single GPU"),
+                   "shard_plan_rank0": step.plan, "lengths_varlen": step.var.lengths_q,
                    "l2": "flushed between steps (256 MB write outside the step's events); "
                          "step inputs also exceed L2",
                    "ms_wall_timed_region": (t_wall1 - t_wall0) * 1e3},
@@ -849,6 +923,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--parts", default="vision,varlen,topk,sparse",
                     help="subset of the step to run (profiling); default: the whole hot path")
+    ap.add_argument("--shard", action="store_true",
+                    help="split one step's units over the ranks (strong scaling) instead of "
+                         "running one whole step per rank (weak scaling, the default)")
+    ap.add_argument("--gather", action="store_true",
+                    help="with --shard: all-gather every rank's results inside the step")
     ap.add_argument("--small", action="store_true",
                     help="profiling-sized varlen batch (4 sequences, 10096 tokens)")
     args = ap.parse_args()
