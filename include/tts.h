@@ -180,13 +180,16 @@ tts_status tts_topk_select_long(const float* logits, int64_t row_stride, int32_t
  * idx        device int32 [nq, topk]
  * out        device fp32 [nq, num_heads, dv];  lse device fp32 [nq, num_heads] or NULL
  * workspace  device scratch, optional (NULL / 0 bytes: not used). With at least
- *            tts_sparse_workspace_bytes(nq) bytes, the (query, V half) units of the last,
- *            partial wave of CTAs each run as 2 or 4 CTAs over consecutive tiles of the
- *            sorted list, and the last of them to finish merges their unnormalised
- *            results (the online-softmax merge, in part order). The result stays
- *            deterministic and order-invariant; split units round differently from
- *            unsplit ones. Owned by the caller; calls that may overlap on the GPU need
- *            separate workspaces.
+ *            tts_sparse_workspace_bytes(nq) bytes: (1) a first launch writes every
+ *            query's canonical list (validated, sorted, resolved to physical rows) into
+ *            the workspace, so the attention CTAs start gathering at once instead of
+ *            sorting first (same lists, same results bit for bit); (2) the (query,
+ *            V half) units of the last, partial wave of CTAs each run as 2 or 4 CTAs
+ *            over consecutive tiles of the sorted list, and the last of them to finish
+ *            merges their unnormalised results (the online-softmax merge, in part
+ *            order). The result stays deterministic and order-invariant; split units
+ *            round differently from unsplit ones. Owned by the caller; calls that may
+ *            overlap on the GPU need separate workspaces.
  * Built shape: num_heads = 128, dqk = 576, dv = 512, 1 <= topk <= 2048,
  * page_size >= 1 (TTS_ERR_UNSUPPORTED otherwise). q, kv_cache, out and workspace
  * 16-byte aligned.
@@ -252,9 +255,10 @@ tts_status tts_paged_kv_write(const void* kv_new, int64_t ntok, int32_t dim,
                               uint32_t* dev_status, void* stream);
 
 /*
- * Workspace bytes that let tts_sparse_attn_paged split the last wave of nq queries on
- * the current device (0: no split for this shape, or no device). At most about
- * 132 KB per SM.
+ * Workspace bytes for nq queries on the current device (0 for nq <= 0 or without a
+ * device): the partial results of the split last wave (when the shape splits; at most
+ * about 132 KB per SM), then, from the next 256-byte boundary, the canonical lists
+ * (4 bytes per query rounded up to 256, plus nq * 2048 * 4 bytes).
  */
 size_t tts_sparse_workspace_bytes(int32_t nq);
 

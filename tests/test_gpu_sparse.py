@@ -163,3 +163,38 @@ def test_chained_topk_then_sparse(tts):
     ro, rl, _ = oracle.sparse_paged(si.q.float().numpy(), si.kv_cache.float().numpy(),
                                     si.page_table.numpy(), oidx, si.kv_len, si.dv, si.scale)
     assert_close_attn(out.cpu().numpy(), ro, "chained")
+
+
+@pytest.mark.parametrize("nq,kv_len,page_size,topk", [
+    (76, 2590, 64, 2048),   # whole waves only on a 152-SM part: no split either way
+    (3, 20000, 64, 2048),   # bitonic sort path
+    (5, 300, 1, 200),       # one-row pages
+])
+def test_presorted_lists_match_in_kernel_sort(tts, nq, kv_len, page_size, topk):
+    # With a workspace, a first launch writes every query's canonical list and the
+    # attention CTAs read it; without one they sort in the kernel. Same lists, so the
+    # outputs are bitwise equal whenever neither call splits its last wave.
+    inp = W.sparse_inputs(nq=nq, kv_len=kv_len, page_size=page_size, topk=topk,
+                          seed=nq + kv_len + topk)
+    idx = inp.idx.clone()
+    idx[0, :7] = -1            # empty slots and a duplicate survive canonicalisation
+    idx[-1, 5] = idx[-1, 6]
+    q, kv, pt, _ = to_dev(inp)
+    ix = idx.to("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152 and nq == 76:
+        ws = torch.empty(tts.sparse_workspace_bytes(nq), dtype=torch.uint8, device="cuda")
+        a_out, a_lse = tts.sparse_attn_paged(q, kv, pt, ix, inp.kv_len, inp.scale, workspace=ws,
+                                             status=st)
+        b_out, b_lse = tts.sparse_attn_paged(q, kv, pt, ix, inp.kv_len, inp.scale, split=False,
+                                             status=st)
+        assert torch.equal(a_out, b_out) and torch.equal(a_lse, b_lse)
+    a_out, a_lse = tts.sparse_attn_paged(q, kv, pt, ix, inp.kv_len, inp.scale, status=st)
+    tts.check_status(st)
+    ro, rl, bad = ref(inp, idx=idx)
+    assert bad == 0
+    assert_close_attn(a_out.cpu().numpy(), ro, f"presorted nq={nq} kv_len={kv_len}")
+    assert_lse_close(a_lse.cpu().numpy(), rl, "presorted lse")
+    perm = W.permute_rows(idx, seed=7).to("cuda")
+    p_out, p_lse = tts.sparse_attn_paged(q, kv, pt, perm, inp.kv_len, inp.scale)
+    assert torch.equal(p_out, a_out) and torch.equal(p_lse, a_lse)

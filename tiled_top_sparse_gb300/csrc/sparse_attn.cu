@@ -78,6 +78,10 @@ struct SparseParams {
   int n_main, parts;
   float* partial;  // [tail units][parts][kSlotFloats]
   uint32_t* done;  // [tail units], zero at launch
+  // Canonical lists made by the sort launch (nullptr: the attention kernel sorts):
+  // query n's physical rows at sorted_rows + n * kMaxTopk, their count sorted_cnt[n].
+  int32_t* sorted_rows;
+  int32_t* sorted_cnt;
 };
 
 // One TMA copy of four whole rows (tile::gather4): 64 columns of each of rows r0..r3 of a
@@ -94,6 +98,133 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, 
 
 __device__ __forceinline__ int kslab_of(int r, int i) {  // i-th K-only slab (global id)
   return r == 0 ? 4 + i : (i < 4 ? i : 8);
+}
+
+// Canonical order of query n's index list: entries validated (-1 and out-of-range
+// entries dropped, the latter reported), sorted ascending (duplicates kept) and resolved
+// through the page table to physical KV rows. Needs all kThreads threads; scratch holds
+// counts [kv_len] (counting sort, kv_len <= kCountCap), a copy of the page table when it
+// fits, then the sorted list, which *rows points at on return. *s_cnt must be zero on
+// entry (shared); returns the number of valid entries.
+__device__ __forceinline__ int canonical_rows(const SparseParams& p, int n, int32_t* scratch,
+                                              int scratch_ints, int* s_cnt, int* s_wsum,
+                                              const int32_t** rows) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t* idx_row = p.idx + (int64_t)n * p.topk;
+  const int32_t* const ptab = p.page_table + (int64_t)n * p.pt_stride;
+  int kv_len = p.kv_len;
+  if (p.kv_lens != nullptr) {
+    kv_len = p.kv_lens[n];
+    if (kv_len < 0) {  // every entry of this query is then out of range
+      if (tid == 0 && p.dev_status != nullptr) atomicOr(p.dev_status, kDevIndexRange);
+      kv_len = 0;
+    }
+  }
+  const bool by_count = kv_len <= kCountCap;
+  const int n_scan = by_count ? p.topk : p.sort_n;
+  const int n_counts = by_count ? kv_len : 0;
+  const int nlp = p.num_logical_pages;
+  const bool pt_cached = n_counts + nlp + n_scan <= scratch_ints;
+  int32_t* counts = scratch;
+  int32_t* pt = counts + n_counts;
+  int32_t* sorted = pt + (pt_cached ? nlp : 0);
+  // The index loads go out first; their round trip overlaps the zeroing and the
+  // page-table copy.
+  int32_t iv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int j = u * kThreads + tid;
+    iv[u] = (j < p.topk) ? idx_row[j] : -1;
+  }
+  for (int v = tid; v < n_counts; v += kThreads) counts[v] = 0;
+  if (pt_cached)
+    for (int g = tid; g < nlp; g += kThreads) pt[g] = ptab[g];
+  __syncthreads();
+  auto page_of = [&](int g) -> int32_t { return pt_cached ? pt[g] : ptab[g]; };
+  // logical position -> (logical page, offset); shifts for power-of-two page sizes
+  auto lpage = [&](int v) { return p.page_shift >= 0 ? v >> p.page_shift : v / p.page_size; };
+  auto row_of = [&](int v) -> int32_t {
+    const int g = lpage(v);
+    return page_of(g) * p.page_size + (v - g * p.page_size);
+  };
+  int my_valid = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int j = u * kThreads + tid;
+    if (j >= n_scan) continue;
+    const int32_t i = iv[u];
+    int key = 0x7FFFFFFF;
+    if (i != -1 && j < p.topk) {
+      const bool in = i >= 0 && i < kv_len && lpage(i) < nlp;
+      const int32_t pg = in ? page_of(lpage(i)) : -1;
+      if (pg >= 0 && pg < p.num_pages) {
+        key = i;
+        ++my_valid;
+      } else if (p.dev_status != nullptr) {
+        atomicOr(p.dev_status, kDevIndexRange);
+      }
+    }
+    if (by_count) {
+      if (key != 0x7FFFFFFF) atomicAdd(&counts[key], 1);  // integer: order-independent
+    } else {
+      sorted[j] = key;
+    }
+  }
+  if (my_valid) atomicAdd(s_cnt, my_valid);
+  __syncthreads();
+  if (by_count) {
+    // Counting sort: thread t owns a contiguous range of positions; an exclusive scan
+    // of the per-range totals gives where each range's entries start.
+    const int per = (kv_len + kThreads - 1) / kThreads;
+    const int v0 = tid * per, v1 = min(kv_len, v0 + per);
+    int tot = 0;
+    for (int v = v0; v < v1; ++v) tot += counts[v];
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_wsum[w];
+    int pos = before + incl - tot;
+    // The sorted list holds physical KV rows (page-table resolved) in logical order.
+    for (int v = v0; v < v1; ++v) {
+      const int c = counts[v];
+      if (c == 0) continue;
+      const int32_t row = row_of(v);
+      for (int k = 0; k < c; ++k) sorted[pos++] = row;
+    }
+  } else {
+    for (int size = 2; size <= p.sort_n; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < (p.sort_n >> 1); i += kThreads) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool asc = (lo & size) == 0;
+          const int a = sorted[lo], b = sorted[hi];
+          if ((a > b) == asc) {
+            sorted[lo] = b;
+            sorted[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+  __syncthreads();
+  const int cnt = *s_cnt;
+  if (!by_count) {  // the bitonic path sorted logical positions: resolve them now
+    for (int pos = tid; pos < cnt; pos += kThreads) {
+      const int32_t v = sorted[pos];
+      sorted[pos] = row_of(v);
+    }
+    __syncthreads();
+  }
+  *rows = sorted;
+  return cnt;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -162,126 +293,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sV0 + i * kQSlabBytes, &qmap, smem_u32(&bar_qlo_smem), 64 * (4 * r + i), 0, n);
   }
 
-  // ---- canonical order: validate, then sort the index list ascending ----
-  // Scratch in the (still unused) K stages: counts [kv_len] (counting sort only), a copy
-  // of the page table when it fits, then the sorted list.
-  const int32_t* idx_row = p.idx + (int64_t)n * p.topk;
-  const int32_t* const ptab = p.page_table + (int64_t)n * p.pt_stride;
-  int kv_len = p.kv_len;
-  if (p.kv_lens != nullptr) {
-    kv_len = p.kv_lens[n];
-    if (kv_len < 0) {  // every entry of this query is then out of range
-      if (tid == 0 && p.dev_status != nullptr) atomicOr(p.dev_status, kDevIndexRange);
-      kv_len = 0;
-    }
-  }
-  const bool by_count = kv_len <= kCountCap;
-  const int n_scan = by_count ? p.topk : p.sort_n;
-  const int n_counts = by_count ? kv_len : 0;
-  const int nlp = p.num_logical_pages;
-  const bool pt_cached = n_counts + nlp + n_scan <= kScratchInts;
-  int32_t* counts = reinterpret_cast<int32_t*>(smem + kQhiBytes);
-  int32_t* pt = counts + n_counts;
-  int32_t* sorted = pt + (pt_cached ? nlp : 0);
-  // The index loads go out first; their round trip overlaps the zeroing and the
-  // page-table copy.
-  int32_t iv[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int j = u * kThreads + tid;
-    iv[u] = (j < p.topk) ? idx_row[j] : -1;
-  }
-  for (int v = tid; v < n_counts; v += kThreads) counts[v] = 0;
-  if (pt_cached)
-    for (int g = tid; g < nlp; g += kThreads) pt[g] = ptab[g];
-  __syncthreads();
-  auto page_of = [&](int g) -> int32_t { return pt_cached ? pt[g] : ptab[g]; };
-  // logical position -> (logical page, offset); shifts for power-of-two page sizes
-  auto lpage = [&](int v) { return p.page_shift >= 0 ? v >> p.page_shift : v / p.page_size; };
-  auto row_of = [&](int v) -> int32_t {
-    const int g = lpage(v);
-    return page_of(g) * p.page_size + (v - g * p.page_size);
-  };
-  int my_valid = 0;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int j = u * kThreads + tid;
-    if (j >= n_scan) continue;
-    const int32_t i = iv[u];
-    int key = 0x7FFFFFFF;
-    if (i != -1 && j < p.topk) {
-      const bool in = i >= 0 && i < kv_len && lpage(i) < nlp;
-      const int32_t pg = in ? page_of(lpage(i)) : -1;
-      if (pg >= 0 && pg < p.num_pages) {
-        key = i;
-        ++my_valid;
-      } else if (p.dev_status != nullptr) {
-        atomicOr(p.dev_status, kDevIndexRange);
-      }
-    }
-    if (by_count) {
-      if (key != 0x7FFFFFFF) atomicAdd(&counts[key], 1);  // integer: order-independent
-    } else {
-      sorted[j] = key;
-    }
-  }
-  if (my_valid) atomicAdd(&s_cnt, my_valid);
-  __syncthreads();
-  if (by_count) {
-    // Counting sort: thread t owns a contiguous range of positions; an exclusive scan
-    // of the per-range totals gives where each range's entries start.
-    const int per = (kv_len + kThreads - 1) / kThreads;
-    const int v0 = tid * per, v1 = min(kv_len, v0 + per);
-    int tot = 0;
-    for (int v = v0; v < v1; ++v) tot += counts[v];
-    int incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w) before += s_wsum[w];
-    int pos = before + incl - tot;
-    // The sorted list holds physical KV rows (page-table resolved) in logical order.
-    for (int v = v0; v < v1; ++v) {
-      const int c = counts[v];
-      if (c == 0) continue;
-      const int32_t row = row_of(v);
-      for (int k = 0; k < c; ++k) sorted[pos++] = row;
-    }
+  // ---- canonical order: the query's index list validated, sorted ascending and
+  // resolved to physical rows -- by the sort launch (in the workspace) or here (in the
+  // still unused K stages) ----
+  const int32_t* sorted;
+  int cnt;
+  if (p.sorted_rows != nullptr) {
+    sorted = p.sorted_rows + (int64_t)n * kMaxTopk;
+    cnt = p.sorted_cnt[n];
   } else {
-    for (int size = 2; size <= p.sort_n; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < (p.sort_n >> 1); i += kThreads) {
-          const int lo = 2 * i - (i & (stride - 1));
-          const int hi = lo + stride;
-          const bool asc = (lo & size) == 0;
-          const int a = sorted[lo], b = sorted[hi];
-          if ((a > b) == asc) {
-            sorted[lo] = b;
-            sorted[hi] = a;
-          }
-        }
-        __syncthreads();
-      }
-    }
+    cnt = canonical_rows(p, n, reinterpret_cast<int32_t*>(smem + kQhiBytes), kScratchInts, &s_cnt,
+                         s_wsum, &sorted);
   }
-  __syncthreads();
-  const int cnt = s_cnt;
   const int n_tiles = (cnt + kTileN - 1) / kTileN;
   // This CTA's tiles of the sorted list (all of them unless the unit is split).
   const int t_begin = part * n_tiles / nparts;
   const int nt = (part + 1) * n_tiles / nparts - t_begin;
-  if (!by_count) {  // the bitonic path sorted logical positions: resolve them now
-    for (int pos = tid; pos < cnt; pos += kThreads) {
-      const int32_t v = sorted[pos];
-      sorted[pos] = row_of(v);
-    }
-    __syncthreads();
-  }
   // Producer warp w keeps, in registers, the physical rows of entries 16 * (w & 3) ..
   // +15 of every tile: lane l holds entry l & 15 of the even tiles (l < 16) or of the
   // odd tiles (l >= 16), oldest first, and drops the front one once that tile is issued.
@@ -660,6 +687,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The canonical lists of every query ahead of the attention launch, one CTA per query,
+// so that the attention CTAs start gathering at once instead of sorting first.
+__global__ void __launch_bounds__(kThreads)
+    sparse_sort_kernel(const SparseParams p, int scratch_ints) {
+  extern __shared__ int32_t scratch[];
+  __shared__ int s_cnt;
+  __shared__ int s_wsum[kThreads / 32];
+  const int n = blockIdx.x;
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  const int32_t* rows;
+  const int cnt = canonical_rows(p, n, scratch, scratch_ints, &s_cnt, s_wsum, &rows);
+  int32_t* dst = p.sorted_rows + (int64_t)n * kMaxTopk;
+  for (int i = threadIdx.x; i < cnt; i += kThreads) dst[i] = rows[i];
+  if (threadIdx.x == 0) p.sorted_cnt[n] = cnt;
+}
+
 // The split of the last wave: with U = 2 nq units on `sms` SMs, the U mod sms units of
 // the partial wave run as `parts` CTAs each (4 if they still fit in one wave, else 2).
 struct SplitPlan {
@@ -684,7 +728,15 @@ SplitPlan plan_split(int nq, int sms) {
 
 }  // namespace
 
-size_t sparse_split_workspace_bytes(int nq, int sms) { return plan_split(nq, sms).bytes; }
+// Workspace layout: the split region (when the shape splits), then from the next 256-byte
+// boundary the canonical lists: counts [nq] (rounded up to 256 bytes), rows [nq][kMaxTopk].
+size_t sorted_lists_bytes(int nq) {
+  return ((size_t)nq * 4 + 255) / 256 * 256 + (size_t)nq * kMaxTopk * 4;
+}
+
+size_t sparse_split_workspace_bytes(int nq, int sms) {
+  return (plan_split(nq, sms).bytes + 255) / 256 * 256 + sorted_lists_bytes(nq);
+}
 
 cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t stream) {
   if (a.heads != kHeads || a.dqk != kDqk || a.dv != kDv || a.topk > kMaxTopk)
@@ -752,6 +804,8 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
   p.parts = 1;
   p.partial = nullptr;
   p.done = nullptr;
+  p.sorted_rows = nullptr;
+  p.sorted_cnt = nullptr;
   int grid = units;
   if (a.workspace != nullptr) {
     int dev = 0, sms = 0;
@@ -759,6 +813,30 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
     if (ea == cudaSuccess) ea = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (ea != cudaSuccess) return ea;
     const SplitPlan sp = plan_split(a.nq, sms);
+    const size_t lists_at = (sp.bytes + 255) / 256 * 256;
+    if (a.workspace_bytes >= lists_at + sorted_lists_bytes(a.nq)) {
+      // The canonical lists first, by a launch of their own (one CTA per query).
+      p.sorted_cnt = reinterpret_cast<int32_t*>(static_cast<char*>(a.workspace) + lists_at);
+      p.sorted_rows = reinterpret_cast<int32_t*>(static_cast<char*>(a.workspace) + lists_at +
+                                                 ((size_t)a.nq * 4 + 255) / 256 * 256);
+      // Scratch: counts (counting sort), the page table when it fits, the list; with one
+      // length for every query its need is known here, else the largest.
+      int scratch_ints = kScratchInts;
+      if (a.kv_lens == nullptr) {
+        const int n_counts = a.kv_len <= kCountCap ? a.kv_len : 0;
+        const int n_scan = a.kv_len <= kCountCap ? a.topk : sort_n;
+        const int want = n_counts + a.num_logical_pages + n_scan;
+        scratch_ints = want < kScratchInts ? want : kScratchInts;
+        if (scratch_ints < n_counts + n_scan) scratch_ints = n_counts + n_scan;
+      }
+      const size_t sort_smem = (size_t)scratch_ints * 4;
+      ea = cudaFuncSetAttribute(sparse_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sort_smem);
+      if (ea != cudaSuccess) return ea;
+      sparse_sort_kernel<<<a.nq, kThreads, sort_smem, stream>>>(p, scratch_ints);
+      ea = cudaGetLastError();
+      if (ea != cudaSuccess) return ea;
+    }
     if (sp.parts > 1 && a.workspace_bytes >= sp.bytes) {
       p.done = static_cast<uint32_t*>(a.workspace);
       p.partial = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + sp.done_bytes);
