@@ -433,7 +433,7 @@ def topk_long_protocol(step, dev, peaks):
     gbs = nbytes / (us * 1e-6) / 1e9
     del sets, ws, lg
     return {"workload": f"{rows} rows x {cols} (last queries of a {cols}-token context), k {k}",
-            "us_per_call": us, "launches_per_call": 7, "bytes": nbytes, "gbs": gbs,
+            "us_per_call": us, "launches_per_call": 3, "bytes": nbytes, "gbs": gbs,
             "frac_hbm": gbs / peaks["hbm_gbs"],
             "protocol": f"CUDA graph of {n_call} calls over 4 rotating input sets"}
 

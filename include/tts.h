@@ -138,9 +138,15 @@ tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows
  * Top-k over long rows: the same result as tts_topk_select (same definition,
  * tie rule and output layout, see above) for rows of any length up to 2^30,
  * such as the long-context indexer rows of "从 SGLang Kernel源码到 GPU Trace"
- * (section 2.2). Each row is split over many CTAs: three histogram passes of a
- * radix select (integer atomics only), a collect pass that ranks ties by
- * position, and a per-row sort of the k picks, so the result is deterministic.
+ * (section 2.2). Sample-select in three launches: per row, a threshold key from a
+ * sample of the window (1/32 of it at most); one pass over the window, split over
+ * many CTAs, that keeps every value at or above the threshold (integer atomics
+ * only); per row, a selection of the k largest kept values by (value, position)
+ * and a sort of them. A row the sample misjudges (fewer than min(k, len) kept,
+ * or more than 16384, e.g. a row piling up on one value) is instead finished
+ * exactly by one CTA straight from the window (radix select, ties ranked by
+ * position): correct for every input, but a few passes over the row at one SM's
+ * bandwidth. The result is deterministic.
  *
  * workspace  device scratch of at least tts_topk_long_workspace_bytes(rows,
  *            row_stride, k) bytes, 16-byte aligned, owned by the caller and

@@ -7,27 +7,28 @@
 // long as the long-context indexer rows of "从 SGLang Kernel源码到 GPU Trace"
 // (section 2.2), where one row no longer fits a CTA.
 //
-// Each row is cut into chunks of kChunk values, one CTA per (row, chunk). Values map to
-// order-preserving 32-bit keys (-0 folded onto +0); a key and its position travel as the
-// 64-bit composite key << 32 | ~position, which orders exactly as the definition does
-// (key descending, then position ascending) and is unique. Launches, in stream order:
-//   1. pass 0: histogram of the keys' top byte, per chunk (kept) and per row (integer
-//      atomics). The row's histogram fixes the top byte d0 of the k-th key.
-//   2. compact: keys whose top byte is above d0 are picks (fewer than k of them); keys
-//      whose top byte is d0 are the candidates, copied as composites into a per-row list
-//      in position order (each chunk's offset comes from the kept chunk histograms, each
-//      warp's from a block scan). Only these two launches read the rows.
-//   3. passes 1-3 over the candidates: histograms of the next three bytes among the
-//      candidates matching the digits chosen so far. Every CTA re-derives those digits
-//      from the earlier histograms (the same scan on the same integers, so all CTAs
-//      agree). After pass 3 the key T of rank k is known, and so is how many candidates
-//      equal to T are still needed; pass 3 keeps each chunk's own histogram too.
-//   4. collect: each candidate chunk picks its keys > T and its first m keys == T in
-//      list (= position) order, m = the ties still needed minus those of the earlier
-//      chunks, clamped to its own count; only the chunk where the cut falls ranks ties.
-//   5. sort: one CTA per row sorts its k composites descending (bitonic network).
-// No float arithmetic decides anything and no CTA waits for another; atomics only
-// change the slot order of the picks, which the final sort removes.
+// Values map to order-preserving 32-bit keys (-0 folded onto +0); a key and its position
+// travel as the 64-bit composite key << 32 | ~position, which orders exactly as the
+// definition does (key descending, then position ascending) and is unique. Sample-select,
+// two launches in stream order (after a reset of the per-row counts):
+//   1. sample: every CTA of a row reads the same 32-value blocks spread evenly over the
+//      window (4096 values at most), histograms their keys' top 12 bits and takes as
+//      threshold t the lower bound of the bucket where the sample's count from the top
+//      reaches the share of 1.5 * min(k, len) + 256 values; windows of up to kCap values
+//      take t = 0. So all CTAs of a row agree on t without waiting for one another.
+//   2. compact: one CTA per (row, chunk) streams the window once and appends every
+//      composite with key >= t to the row's candidate array (gathered per CTA in shared
+//      memory, placed by one integer atomic per CTA: the order in the array is
+//      arbitrary, its contents are not).
+//   3. finish: one CTA per row. If the candidates hold at least min(k, len) composites
+//      and fit the array, every selected composite is among them (at least min(k, len)
+//      keys are >= t, so the min(k, len)-th largest key is too): an MSB-first radix
+//      select over the 64-bit composites finds the min(k, len)-th largest, C; the
+//      composites >= C are sorted descending (bitonic network) and their positions
+//      written. Else (the sample misjudged the row, e.g. a row piling up on one value)
+//      the CTA finds the picks exactly on its own: a radix select over the window's
+//      keys, a collect that ranks ties by position, and the same sort.
+// Either way the result is fully determined by the input, and no CTA waits for another.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -37,43 +38,26 @@
 namespace tts {
 namespace {
 
-constexpr int kLThreads = 512;
+constexpr int kCap = 16384;           // candidates kept per row
+constexpr int kLThreads = 512;        // sample and compact CTAs
 constexpr int kLWarps = kLThreads / 32;
-constexpr int kChunk = 16384;                  // window values per CTA
-constexpr int kUnroll = 8;                     // loads in flight per thread
-constexpr int kBins = 256;                     // one byte of the key per pass
-constexpr int kPasses = 4;
-__host__ __device__ constexpr int shift_of(int pass) { return 24 - 8 * pass; }
+constexpr int kChunkQuantum = 4096;   // compact chunks are multiples of this many values
+constexpr int kUnroll = 8;            // loads in flight per thread (scalar path)
+constexpr int kUnroll4 = 4;           // float4 loads in flight per thread (vector path)
+constexpr int kSampleBlocks = 128;    // 32-value sample blocks per row, at most
+constexpr int kSampleBits = 12;       // key bits of the sample histogram
+constexpr int kFinishThreads = 1024;
+constexpr int kMaxTake = 4096;        // k <= 4096
+constexpr int kFWarps = kFinishThreads / 32;
 
-// Per-row workspace: ints h [4][256], count [4], chunk histograms of pass 0 and of
-// pass 3 [G][256] each (zeroed per call); then the picks (uint64) [k] and the candidate
-// list (uint64) [row_stride].
-struct RowWs {
-  int* h[kPasses];
-  int* count;
-  int* chunk_h0;
-  int* chunk_h3;
-  uint64_t* cand;
-  uint64_t* list;
-};
-__host__ __device__ __forceinline__ int64_t zeroed_bytes(int g) {
-  return (((int64_t)kBins * kPasses + 4 + 2 * (int64_t)g * kBins) * 4 + 15) & ~int64_t(15);
+// Per-row workspace: header {threshold key, candidate count, 2 spare} then kCap
+// composites.
+constexpr int64_t kRowBytes = 16 + 8 * (int64_t)kCap;
+__host__ __device__ __forceinline__ uint32_t* row_head(uint8_t* ws, int64_t row) {
+  return reinterpret_cast<uint32_t*>(ws + row * kRowBytes);
 }
-__host__ __device__ __forceinline__ int64_t row_bytes(int g, int k, int64_t row_stride) {
-  return zeroed_bytes(g) + 8 * ((int64_t)k + (k & 1)) + 8 * (row_stride + (row_stride & 1));
-}
-__device__ __forceinline__ RowWs row_ws(uint8_t* ws, int64_t row, int g, int k,
-                                        int64_t row_stride) {
-  uint8_t* b = ws + row * row_bytes(g, k, row_stride);
-  int* bi = reinterpret_cast<int*>(b);
-  RowWs w;
-  for (int p = 0; p < kPasses; ++p) w.h[p] = bi + p * kBins;
-  w.count = bi + kPasses * kBins;
-  w.chunk_h0 = w.count + 4;
-  w.chunk_h3 = w.chunk_h0 + (int64_t)g * kBins;
-  w.cand = reinterpret_cast<uint64_t*>(b + zeroed_bytes(g));
-  w.list = w.cand + k + (k & 1);
-  return w;
+__host__ __device__ __forceinline__ uint64_t* row_cand(uint8_t* ws, int64_t row) {
+  return reinterpret_cast<uint64_t*>(ws + row * kRowBytes + 16);
 }
 
 __device__ __forceinline__ uint32_t key_of(float x) {
@@ -81,8 +65,15 @@ __device__ __forceinline__ uint32_t key_of(float x) {
   if ((u & 0x7FFFFFFFu) == 0) u = 0;  // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ uint64_t comp_of(uint32_t key, int64_t pos) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
+}
+__device__ __forceinline__ bool window_ok(int64_t st, int64_t len, int64_t row_stride) {
+  return st >= 0 && len >= 0 && st + len <= row_stride;
+}
 
-// Block-wide exclusive scan of one int per thread; *total = the block's sum.
+// Block-wide exclusive scan of one int per thread (NW warps); *total = the block's sum.
+template <int NW>
 __device__ __forceinline__ int scan_excl(int v, int* warp_tot, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -94,377 +85,158 @@ __device__ __forceinline__ int scan_excl(int v, int* warp_tot, int* total) {
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int t = (lane < kLWarps) ? warp_tot[lane] : 0;
+    int t = (lane < NW) ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xFFFFFFFFu, t, o);
       if (lane >= o) t += y;
     }
-    if (lane < kLWarps) warp_tot[lane] = t;
+    if (lane < NW) warp_tot[lane] = t;
   }
   __syncthreads();
   const int before = (warp > 0) ? warp_tot[warp - 1] : 0;
-  *total = warp_tot[kLWarps - 1];
+  *total = warp_tot[NW - 1];
   __syncthreads();
   return before + x - v;
 }
 
-// The digit d of a descending histogram walk at which `remaining` is reached:
-// count(bins > d) < remaining <= count(bins >= d). Thread t owns bins 255-8t down to
-// 248-8t. Returns d; *above = count(bins > d). Block-collective.
-__device__ int pick_digit(const int* hist, int remaining, int* warp_tot, int* s_pick,
-                          int* above) {
-  const int t = threadIdx.x;
-  int c[8], s = 0;
+// ---------------------------------------------------------------------------- 1. sample
+// The row's threshold key from its sample (block-collective; every CTA of a row computes
+// the same value from the same values): the lower bound of the 12-bit key bucket where
+// the sample's count from the top reaches its share of 1.5 * take + 256 values.
+__device__ uint32_t sample_threshold(const float* __restrict__ x, int64_t len, int64_t take,
+                                     uint32_t* hist, int* warp_tot, uint32_t* s_t) {
+  int64_t nb = len / 32;
+  if (nb > kSampleBlocks) nb = kSampleBlocks;
+  const int64_t stride = len / nb;  // >= 32
+  const int64_t ns = 32 * nb;
+  int64_t want = ((3 * take / 2 + 256) * ns + len - 1) / len;  // rounded up
+  if (want > ns) want = ns;
+  for (int b = threadIdx.x; b < (1 << kSampleBits); b += kLThreads) hist[b] = 0u;
+  if (threadIdx.x == 0) *s_t = 0u;  // sample too small to reach `want`: every key
+  __syncthreads();
+  // ns is a multiple of 32, so every lane of a warp takes the same number of steps.
+  for (int64_t s = threadIdx.x; s < ns; s += kLThreads) {
+    const int64_t j = (s >> 5) * stride + (s & 31);
+    const uint32_t b = key_of(__ldg(x + j)) >> (32 - kSampleBits);
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);  // one atomic per bucket
+    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[b], (uint32_t)__popc(peers));
+  }
+  __syncthreads();
+  // Descending walk: thread t owns buckets 4095 - 8t down to 4088 - 8t.
+  constexpr int kPer = (1 << kSampleBits) / kLThreads;
+  uint32_t c[kPer];
+  int sum = 0;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int b = kBins - 1 - 8 * t - q;
-    c[q] = (8 * t < kBins) ? __ldcg(hist + b) : 0;
-    s += c[q];
+  for (int q = 0; q < kPer; ++q) {
+    c[q] = hist[(1 << kSampleBits) - 1 - kPer * threadIdx.x - q];
+    sum += (int)c[q];
   }
   int tot;
-  int run = scan_excl(s, warp_tot, &tot);
+  int run = scan_excl<kLWarps>(sum, warp_tot, &tot);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    if (run < remaining && remaining <= run + c[q]) {
-      s_pick[0] = kBins - 1 - 8 * t - q;
-      s_pick[1] = run;
-    }
-    run += c[q];
+  for (int q = 0; q < kPer; ++q) {
+    if (run < want && want <= run + (int)c[q])
+      *s_t = (uint32_t)((1 << kSampleBits) - 1 - kPer * (int)threadIdx.x - q) << (32 - kSampleBits);
+    run += (int)c[q];
   }
   __syncthreads();
-  const int d = s_pick[0];
-  *above = s_pick[1];
-  __syncthreads();
-  return d;
+  return *s_t;
 }
 
-struct Sel {
-  uint32_t prefix, mask;
-  int remaining;
-};
-// The digits chosen by passes [0, upto): block-collective, identical in every CTA.
-__device__ Sel chosen(const RowWs& w, int k, int upto, int* warp_tot, int* s_pick) {
-  Sel s{0u, 0u, k};
-  for (int q = 0; q < upto; ++q) {
-    int above;
-    const int d = pick_digit(w.h[q], s.remaining, warp_tot, s_pick, &above);
-    s.remaining -= above;
-    s.prefix |= static_cast<uint32_t>(d) << shift_of(q);
-    s.mask |= static_cast<uint32_t>(kBins - 1) << shift_of(q);
-  }
-  return s;
-}
-
-__device__ __forceinline__ bool window_ok(int64_t st, int64_t len, int64_t row_stride) {
-  return st >= 0 && len >= 0 && st + len <= row_stride;
-}
-
-// Where a CTA's keys come from: the row itself (pass 0, compact) or the row's candidate
-// list (passes 1-3, collect). Both give (key, composite) for an index of the range.
-struct RowSrc {
-  const float* x;  // the window, or nullptr for the list
-  const uint64_t* list;
-  __device__ __forceinline__ uint64_t get(int64_t j) const {
-    if (x != nullptr) {
-      const uint32_t key = key_of(__ldg(x + j));
-      return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~j);
-    }
-    return __ldcg(list + j);
-  }
-};
-
-// Per (row, chunk) setup shared by the kernels. Returns false for an invalid window. The
-// chunks cut the window; over the candidate list the kernel sets the range itself
-// (in_list) once it knows the list's length.
-struct Job {
-  int64_t row, c0, c1;
-  int chunk;
-  bool all;  // len <= k: every value of the window is a pick
-  RowWs w;
-  RowSrc src;
-};
-template <bool kList>
-__device__ __forceinline__ bool setup(Job& jb, const float* logits, int64_t row_stride,
-                                      const int32_t* row_starts, const int32_t* row_lens,
-                                      int k, int g, uint8_t* ws) {
-  jb.row = blockIdx.x / g;
-  jb.chunk = blockIdx.x % g;
-  const int64_t st = row_starts[jb.row], len = row_lens[jb.row];
-  if (!window_ok(st, len, row_stride)) return false;
-  jb.all = len <= k;
-  jb.w = row_ws(ws, jb.row, g, k, row_stride);
-  jb.src.x = kList ? nullptr : logits + jb.row * row_stride + st;
-  jb.src.list = jb.w.list;
-  jb.c0 = (int64_t)jb.chunk * kChunk;
-  jb.c1 = (jb.c0 + kChunk < len) ? jb.c0 + kChunk : len;
-  return true;
-}
-// Over the candidate list: its length, which the compact launch records in count[1].
-__device__ __forceinline__ void in_list(Job& jb) {
-  const int64_t n = __ldcg(jb.w.count + 1);
-  jb.c1 = (jb.c0 + kChunk < n) ? jb.c0 + kChunk : n;
-}
-
-// Histogram of key byte `pass` over the CTA's range, among keys matching the digits
-// chosen by the earlier passes; added to the row's histogram, and kept per chunk for
-// passes 0 and 3.
-template <bool kList>
-__global__ void __launch_bounds__(kLThreads) topk_long_hist_kernel(
+// ---------------------------------------------------------------------------- 2. compact
+// One CTA per (row, chunk): the row's threshold (windows of up to kCap values: every
+// key), then one pass over the chunk. The CTA gathers its candidates in shared memory,
+// reserves their place in the row's array with one atomic, and copies them there; a CTA
+// with more than kLocal candidates adds kCap + 1 to the count instead, which sends its
+// row to the exact path.
+constexpr int kLocal = 3072;
+__global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
     const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
-    const int32_t* __restrict__ row_lens, int k, int g, int pass, uint8_t* ws,
-    uint32_t* status) {
-  __shared__ int whist[kLWarps][kBins];  // one histogram per warp: atomics stay in-warp
+    const int32_t* __restrict__ row_lens, int k, int g, int64_t chunk_len, uint8_t* ws) {
+  __shared__ uint64_t local[kLocal];
+  __shared__ uint32_t hist[1 << kSampleBits];
   __shared__ int warp_tot[kLWarps];
-  __shared__ int s_pick[2];
-  Job jb;
-  if (!setup<kList>(jb, logits, row_stride, row_starts, row_lens, k, g, ws)) {
-    if (!kList && blockIdx.x % g == 0 && threadIdx.x == 0 && status != nullptr) {
-      const int64_t r = blockIdx.x / g, st = row_starts[r], len = row_lens[r];
-      if (!window_ok(st, len, row_stride)) atomicOr(status, kDevIndexRange);
-    }
-    return;
-  }
-  if (jb.all) return;
-  if (kList) {
-    in_list(jb);
-    if (jb.c0 >= jb.c1) return;  // beyond the list (its chunk histograms stay zero)
-  }
-  const Sel sel = chosen(jb.w, k, pass, warp_tot, s_pick);
-  const int shift = shift_of(pass);
-  for (int b = threadIdx.x; b < kLWarps * kBins; b += kLThreads) (&whist[0][0])[b] = 0;
-  __syncthreads();
-  int* const my = whist[threadIdx.x >> 5];
-  for (int64_t j0 = jb.c0; j0 < jb.c1; j0 += kLThreads * kUnroll) {
-    uint32_t v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t j = j0 + u * kLThreads + threadIdx.x;
-      if (kList)
-        v[u] = (j < jb.c1) ? static_cast<uint32_t>(__ldcg(jb.src.list + j) >> 32) : 0u;
-      else
-        v[u] = (j < jb.c1) ? key_of(__ldg(jb.src.x + j)) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t j = j0 + u * kLThreads + threadIdx.x;
-      const uint32_t key = v[u];
-      const bool active = j < jb.c1 && (key & sel.mask) == sel.prefix;
-      if (active) atomicAdd(&my[(key >> shift) & (kBins - 1)], 1);  // this warp's own bins
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < kBins) {
-    int v = 0;
-#pragma unroll
-    for (int q = 0; q < kLWarps; ++q) v += whist[q][threadIdx.x];
-    if (v != 0) atomicAdd(jb.w.h[pass] + threadIdx.x, v);
-    int* keep = pass == 0 ? jb.w.chunk_h0 : (pass == kPasses - 1 ? jb.w.chunk_h3 : nullptr);
-    if (keep != nullptr) keep[(int64_t)jb.chunk * kBins + threadIdx.x] = v;
-  }
-}
-
-// Picks gathered in shared memory (warp-aggregated slots), then sent to the row's pick
-// array behind one atomic per CTA.
-struct PickBuf {
-  uint64_t* s;
-  int* s_n;
-  int k;
-  uint32_t* status;
-  __device__ __forceinline__ void put(bool pick, uint64_t comp) const {
-    const int lane = threadIdx.x & 31;
-    const uint32_t b = __ballot_sync(0xFFFFFFFFu, pick);
-    int base = 0;
-    if (lane == 0 && b != 0) base = atomicAdd(s_n, __popc(b));
-    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-    if (pick) {
-      const int slot = base + __popc(b & ((1u << lane) - 1u));
-      if (slot < k)
-        s[slot] = comp;
-      else if (status != nullptr)
-        atomicOr(status, kDevBadArg);  // never: a row has exactly min(k, len) picks
-    }
-  }
-};
-__device__ __forceinline__ void flush_picks(const PickBuf& pb, const RowWs& w, int* s_base) {
-  __syncthreads();
-  const int n = *pb.s_n < pb.k ? *pb.s_n : pb.k;
-  if (threadIdx.x == 0) *s_base = n > 0 ? atomicAdd(w.count, n) : 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < n; i += kLThreads) {
-    if (*s_base + i < pb.k)
-      w.cand[*s_base + i] = pb.s[i];
-    else if (pb.status != nullptr)
-      atomicOr(pb.status, kDevBadArg);
-  }
-}
-
-// Keys with a top byte above the k-th key's are picks; those with its top byte go to the
-// candidate list, in position order.
-__global__ void __launch_bounds__(kLThreads) topk_long_compact_kernel(
-    const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
-    const int32_t* __restrict__ row_lens, int k, int g, uint8_t* ws, uint32_t* status) {
-  extern __shared__ __align__(16) uint64_t picks[];  // [k]
-  __shared__ int warp_tot[kLWarps];
-  __shared__ int s_pick[2];
-  __shared__ int s_n, s_base;
-  Job jb;
-  if (!setup<false>(jb, logits, row_stride, row_starts, row_lens, k, g, ws)) return;
-  if (jb.c0 >= jb.c1) return;
-  if (threadIdx.x == 0) s_n = 0;
-  __syncthreads();
-  const PickBuf pb{picks, &s_n, k, status};
-  if (jb.all) {
-    for (int64_t j0 = jb.c0; j0 < jb.c1; j0 += kLThreads) {
-      const int64_t j = j0 + threadIdx.x;
-      pb.put(j < jb.c1, j < jb.c1 ? jb.src.get(j) : 0ull);
-    }
-    flush_picks(pb, jb.w, &s_base);
-    return;
-  }
-  const Sel sel = chosen(jb.w, k, 1, warp_tot, s_pick);
-  const uint32_t d0 = sel.prefix >> 24;
-  if (jb.chunk == 0 && threadIdx.x == 0) jb.w.count[1] = __ldcg(jb.w.h[0] + d0);
-  int part = 0;  // candidates in the chunks before this one
-  for (int c = threadIdx.x; c < jb.chunk; c += kLThreads)
-    part += __ldcg(jb.w.chunk_h0 + (int64_t)c * kBins + d0);
-  int base;
-  scan_excl(part, warp_tot, &base);
-  // each warp owns a contiguous slice: count its candidates, scan, then write them
-  constexpr int kSlice = kChunk / kLWarps;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t s0 = jb.c0 + (int64_t)warp * kSlice;
-  const int64_t s1 = (s0 + kSlice < jb.c1) ? s0 + kSlice : jb.c1;
-  const float* x = jb.src.x;
-  int mine = 0;
-  for (int64_t j0 = s0; j0 < s1; j0 += 32 * kUnroll) {
-    float v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t j = j0 + 32 * u + lane;
-      v[u] = (j < s1) ? __ldg(x + j) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t j = j0 + 32 * u + lane;
-      mine += __popc(__ballot_sync(0xFFFFFFFFu, j < s1 && (key_of(v[u]) >> 24) == d0));
-    }
-  }
-  int tot;
-  int at = scan_excl(lane == 0 ? mine : 0, warp_tot, &tot);
-  at = base + __shfl_sync(0xFFFFFFFFu, at, 0);
-  for (int64_t j0 = s0; j0 < s1; j0 += 32 * kUnroll) {
-    float v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t j = j0 + 32 * u + lane;
-      v[u] = (j < s1) ? __ldg(x + j) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t j = j0 + 32 * u + lane;
-      const uint32_t key = key_of(v[u]);
-      const uint64_t comp = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~j);
-      const uint32_t top = key >> 24;
-      const bool cand = j < s1 && top == d0;
-      const uint32_t b = __ballot_sync(0xFFFFFFFFu, cand);
-      if (cand) jb.w.list[at + __popc(b & ((1u << lane) - 1u))] = comp;
-      at += __popc(b);
-      pb.put(j < s1 && top > d0, comp);
-    }
-  }
-  flush_picks(pb, jb.w, &s_base);
-}
-
-// Candidates > T, and the first m candidates == T of this chunk (list order = position
-// order), are picks.
-__global__ void __launch_bounds__(kLThreads) topk_long_collect_kernel(
-    const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
-    const int32_t* __restrict__ row_lens, int k, int g, uint8_t* ws, uint32_t* status) {
-  extern __shared__ __align__(16) uint64_t picks[];  // [k]
-  __shared__ int warp_tot[kLWarps];
-  __shared__ int s_pick[2];
-  __shared__ int s_n, s_base;
-  Job jb;
-  if (!setup<true>(jb, logits, row_stride, row_starts, row_lens, k, g, ws) || jb.all) return;
-  in_list(jb);
-  if (jb.c0 >= jb.c1) return;
-  const Sel sel = chosen(jb.w, k, kPasses, warp_tot, s_pick);
-  const uint32_t T = sel.prefix;
-  const int lo = T & (kBins - 1);
-  int part = 0;  // ties (keys == T) in the chunks before this one
-  for (int c = threadIdx.x; c < jb.chunk; c += kLThreads)
-    part += __ldcg(jb.w.chunk_h3 + (int64_t)c * kBins + lo);
-  int before;
-  scan_excl(part, warp_tot, &before);
-  const int n_eq = __ldcg(jb.w.chunk_h3 + (int64_t)jb.chunk * kBins + lo);
-  int m = sel.remaining - before;
-  m = m < 0 ? 0 : (m > n_eq ? n_eq : m);
-  if (threadIdx.x == 0) s_n = 0;
-  __syncthreads();
-  const PickBuf pb{picks, &s_n, k, status};
-  if (m == 0 || m == n_eq) {
-    const bool take_eq = m > 0;
-    for (int64_t j0 = jb.c0; j0 < jb.c1; j0 += kLThreads * kUnroll) {
-      uint64_t v[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t j = j0 + u * kLThreads + threadIdx.x;
-        v[u] = (j < jb.c1) ? jb.src.get(j) : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t j = j0 + u * kLThreads + threadIdx.x;
-        const uint32_t key = static_cast<uint32_t>(v[u] >> 32);
-        pb.put(j < jb.c1 && (key > T || (take_eq && key == T)), v[u]);
-      }
-    }
-  } else {  // the chunk where the cut falls: per-warp slices ranked by one block scan
-    constexpr int kSlice = kChunk / kLWarps;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t s0 = jb.c0 + (int64_t)warp * kSlice;
-    const int64_t s1 = (s0 + kSlice < jb.c1) ? s0 + kSlice : jb.c1;
-    int mine = 0;
-    for (int64_t j0 = s0; j0 < s1; j0 += 32) {
-      const int64_t j = j0 + lane;
-      const bool eq = j < s1 && static_cast<uint32_t>(jb.src.get(j) >> 32) == T;
-      mine += __popc(__ballot_sync(0xFFFFFFFFu, eq));
-    }
-    int tot;
-    int rank = scan_excl(lane == 0 ? mine : 0, warp_tot, &tot);
-    rank = __shfl_sync(0xFFFFFFFFu, rank, 0);  // ties before this warp's slice
-    for (int64_t j0 = s0; j0 < s1; j0 += 32) {
-      const int64_t j = j0 + lane;
-      const uint64_t comp = (j < s1) ? jb.src.get(j) : 0ull;
-      const uint32_t key = static_cast<uint32_t>(comp >> 32);
-      const bool eq = j < s1 && key == T;
-      const uint32_t e = __ballot_sync(0xFFFFFFFFu, eq);
-      const int r = rank + __popc(e & ((1u << lane) - 1u));
-      pb.put(j < s1 && (key > T || (eq && r < m)), comp);
-      rank += __popc(e);
-    }
-  }
-  flush_picks(pb, jb.w, &s_base);
-}
-
-constexpr int kSortThreads = 1024;  // one compare-exchange per thread and stage at k = 2048
-__global__ void __launch_bounds__(kSortThreads) topk_long_sort_kernel(
-    const int64_t row_stride, const int32_t* __restrict__ row_starts,
-    const int32_t* __restrict__ row_lens, int k, int g, int sort_n, uint8_t* ws,
-    int32_t* __restrict__ idx) {
-  extern __shared__ __align__(16) uint64_t sel[];  // [sort_n]
-  const int64_t row = blockIdx.x;
+  __shared__ uint32_t s_n, s_base, s_t;
+  const int64_t row = blockIdx.x / g;
+  const int chunk = blockIdx.x % g;
   const int64_t st = row_starts[row], len = row_lens[row];
-  int32_t* out = idx + row * (int64_t)k;
-  const bool ok = window_ok(st, len, row_stride);
-  const int take = ok ? (int)(len < k ? len : k) : 0;
-  const RowWs w = row_ws(ws, row, g, k, row_stride);
-  for (int j = threadIdx.x; j < sort_n; j += kSortThreads)
-    sel[j] = (j < take) ? __ldcg(w.cand + j) : 0ull;  // padding sorts last
+  if (!window_ok(st, len, row_stride)) return;
+  const int64_t c0 = (int64_t)chunk * chunk_len;
+  const int64_t c1 = (c0 + chunk_len < len) ? c0 + chunk_len : len;
+  if (c0 >= c1) return;
+  uint32_t* head = row_head(ws, row);
+  uint64_t* cand = row_cand(ws, row);
+  const float* x = logits + row * row_stride + st;
+  const int64_t take = len < k ? len : k;
+  const uint32_t t = len <= kCap ? 0u : sample_threshold(x, len, take, hist, warp_tot, &s_t);
+  if (threadIdx.x == 0) s_n = 0u;
   __syncthreads();
-  for (int size = 2; size <= sort_n; size <<= 1) {
+  // key(x) >= t  <=>  x >= the float whose key is t (keys order as the floats do, -0 and
+  // +0 alike), so each value costs one float comparison; only the candidates (a few per
+  // cent) compute their key and take a slot. t = 0 takes every value.
+  const bool all = t == 0u;
+  const float tf = __uint_as_float((t & 0x80000000u) ? (t & 0x7FFFFFFFu) : ~t);
+  auto consider = [&](bool valid, float v, int64_t j) {
+    if (valid && (all || v >= tf)) {
+      const uint32_t slot = atomicAdd(&s_n, 1u);
+      if (slot < (uint32_t)kLocal) local[slot] = comp_of(key_of(v), j);
+    }
+  };
+  // Vector loads when the chunk starts on a 16-byte boundary (the whole CTA agrees).
+  if ((reinterpret_cast<uintptr_t>(x + c0) & 15) == 0) {
+    for (int64_t j0 = c0; j0 < c1; j0 += 4 * kLThreads * kUnroll4) {
+      float4 v[kUnroll4];
+#pragma unroll
+      for (int u = 0; u < kUnroll4; ++u) {
+        const int64_t j = j0 + 4 * (u * kLThreads + threadIdx.x);
+        v[u] = (j + 3 < c1) ? __ldg(reinterpret_cast<const float4*>(x + j))
+                            : make_float4(j < c1 ? __ldg(x + j) : 0.f,
+                                          j + 1 < c1 ? __ldg(x + j + 1) : 0.f,
+                                          j + 2 < c1 ? __ldg(x + j + 2) : 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll4; ++u) {
+        const int64_t j = j0 + 4 * (u * kLThreads + threadIdx.x);
+        consider(j < c1, v[u].x, j);
+        consider(j + 1 < c1, v[u].y, j + 1);
+        consider(j + 2 < c1, v[u].z, j + 2);
+        consider(j + 3 < c1, v[u].w, j + 3);
+      }
+    }
+  } else {
+    for (int64_t j0 = c0; j0 < c1; j0 += kLThreads * kUnroll) {
+      float v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t j = j0 + u * kLThreads + threadIdx.x;
+        v[u] = (j < c1) ? __ldg(x + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t j = j0 + u * kLThreads + threadIdx.x;
+        consider(j < c1, v[u], j);
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t n = s_n;
+  if (n == 0) return;
+  if (threadIdx.x == 0)
+    s_base = atomicAdd(head + 1, n <= (uint32_t)kLocal ? n : (uint32_t)kCap + 1u);
+  __syncthreads();
+  if (n > (uint32_t)kLocal) return;
+  const uint32_t base = s_base;
+  for (uint32_t i = threadIdx.x; i < n; i += kLThreads)
+    if (base + i < (uint32_t)kCap) cand[base + i] = local[i];
+}
+
+// ---------------------------------------------------------------------------- 3. finish
+// Bitonic sort of sel[0, n) descending (n a power of two), by the whole block.
+__device__ __forceinline__ void sort_desc(uint64_t* sel, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (sort_n >> 1); i += kSortThreads) {
+      for (int i = threadIdx.x; i < (n >> 1); i += kFinishThreads) {
         const int lo = 2 * i - (i & (stride - 1));
         const int hi = lo + stride;
         const bool desc = (lo & size) == 0;
@@ -477,58 +249,211 @@ __global__ void __launch_bounds__(kSortThreads) topk_long_sort_kernel(
       __syncthreads();
     }
   }
-  for (int j = threadIdx.x; j < k; j += kSortThreads)
-    out[j] = (j < take) ? static_cast<int32_t>(~static_cast<uint32_t>(sel[j] & 0xFFFFFFFFull)) : -1;
 }
 
-int chunks_of(int64_t row_stride) { return (int)((row_stride + kChunk - 1) / kChunk); }
+// Exact selection by one CTA straight from the window: MSB-first radix select (4 x 8
+// bits) of the key of rank `take`, then the picks -- every key above it, and the first
+// ties in position order (block scans) -- into sel[0, take). Returns nothing; sel holds
+// the picks in arbitrary order.
+__device__ void select_exact(const float* __restrict__ x, int64_t len, int take, uint64_t* sel,
+                             int* hist, int* warp_tot, int* s_digit, int* s_above, int* s_n) {
+  uint32_t prefix = 0, mask = 0;
+  int remaining = take;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int b = threadIdx.x; b < 256; b += kFinishThreads) hist[b] = 0;
+    __syncthreads();
+    for (int64_t j = threadIdx.x; j < len; j += kFinishThreads) {
+      const uint32_t key = key_of(__ldg(x + j));
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {  // lane l owns bins 255 - 8l .. 248 - 8l (descending)
+      const int l = threadIdx.x;
+      int c[8], s = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c[q] = hist[255 - 8 * l - q];
+        s += c[q];
+      }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (l >= o) incl += y;
+      }
+      int above = incl - s;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (above < remaining && remaining <= above + c[q]) {
+          *s_digit = 255 - 8 * l - q;
+          *s_above = above;
+        }
+        above += c[q];
+      }
+    }
+    __syncthreads();
+    remaining -= *s_above;
+    prefix |= static_cast<uint32_t>(*s_digit) << shift;
+    mask |= 0xFFu << shift;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;  // take - remaining keys are > T; `remaining` ties needed
+  if (threadIdx.x == 0) *s_n = 0;
+  __syncthreads();
+  int ties_before = 0;
+  for (int64_t j0 = 0; j0 < len; j0 += kFinishThreads) {
+    const int64_t j = j0 + threadIdx.x;
+    const uint32_t key = (j < len) ? key_of(__ldg(x + j)) : 0u;
+    const bool gt = j < len && key > T;
+    const bool eq = j < len && key == T;
+    int tot;
+    const int rank = ties_before + scan_excl<kFWarps>(eq ? 1 : 0, warp_tot, &tot);
+    if (gt || (eq && rank < remaining)) {
+      const int slot = atomicAdd(s_n, 1);
+      if (slot < take) sel[slot] = comp_of(key, j);
+    }
+    ties_before += tot;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
+    const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
+    const int32_t* __restrict__ row_lens, int k, uint8_t* ws, int32_t* __restrict__ idx,
+    uint32_t* status) {
+  extern __shared__ __align__(16) uint64_t sel[];  // [kCap] candidates, [kMaxTake] picks
+  __shared__ int hist[256];
+  __shared__ int warp_tot[kFWarps];
+  __shared__ int s_digit, s_above, s_n;
+  const int64_t row = blockIdx.x;
+  const int64_t st = row_starts[row], len = row_lens[row];
+  int32_t* out = idx + row * (int64_t)k;
+  if (!window_ok(st, len, row_stride)) {
+    if (threadIdx.x == 0 && status != nullptr) atomicOr(status, kDevIndexRange);
+    for (int j = threadIdx.x; j < k; j += kFinishThreads) out[j] = -1;
+    return;
+  }
+  const int take = (int)(len < k ? len : k);
+  const int64_t cnt = (int64_t)__ldcg(row_head(ws, row) + 1);
+  uint64_t* const picks = sel + kCap;  // [kMaxTake]: the selected composites, to sort
+  if (cnt >= take && cnt <= kCap) {
+    const int n = (int)cnt;
+    const uint64_t* cand = row_cand(ws, row);
+    for (int j = threadIdx.x; j < n; j += kFinishThreads) sel[j] = __ldcg(cand + j);
+    __syncthreads();
+    // The take-th largest composite C among the candidates (they are unique): an
+    // MSB-first radix select over the 64 bits, then every composite >= C is a pick.
+    uint64_t prefix = 0, mask = 0;
+    int remaining = take;
+    for (int pass = 0; pass < 8 && n > take; ++pass) {
+      const int shift = 56 - 8 * pass;
+      for (int b = threadIdx.x; b < 256; b += kFinishThreads) hist[b] = 0;
+      __syncthreads();
+      for (int j = threadIdx.x; j < n; j += kFinishThreads) {
+        const uint64_t c = sel[j];
+        if ((c & mask) == prefix) atomicAdd(&hist[(int)((c >> shift) & 0xFFu)], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {  // lane l owns bins 255 - 8l .. 248 - 8l (descending)
+        const int l = threadIdx.x;
+        int c[8], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          c[q] = hist[255 - 8 * l - q];
+          sum += c[q];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (l >= o) incl += y;
+        }
+        int above = incl - sum;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (above < remaining && remaining <= above + c[q]) {
+            s_digit = 255 - 8 * l - q;
+            s_above = above;
+          }
+          above += c[q];
+        }
+      }
+      __syncthreads();
+      remaining -= s_above;
+      prefix |= static_cast<uint64_t>(s_digit) << shift;
+      mask |= 0xFFull << shift;
+      __syncthreads();
+    }
+    const uint64_t C = (n > take) ? prefix : 0ull;  // n == take: every candidate
+    if (threadIdx.x == 0) s_n = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += kFinishThreads) {
+      const uint64_t c = sel[j];
+      if (c >= C) {
+        const int slot = atomicAdd(&s_n, 1);
+        if (slot < take) picks[slot] = c;
+      }
+    }
+  } else {  // the sample misjudged this row: select exactly from the window itself
+    select_exact(logits + row * row_stride + st, len, take, picks, hist, warp_tot, &s_digit,
+                 &s_above, &s_n);
+  }
+  int sort_n = 1;
+  while (sort_n < take) sort_n <<= 1;
+  for (int j = take + threadIdx.x; j < sort_n; j += kFinishThreads) picks[j] = 0ull;  // last
+  __syncthreads();
+  sort_desc(picks, sort_n);
+  uint64_t* const sel_out = picks;
+  for (int j = threadIdx.x; j < k; j += kFinishThreads)
+    out[j] = (j < take) ? static_cast<int32_t>(~static_cast<uint32_t>(sel_out[j] & 0xFFFFFFFFull))
+                        : -1;
+}
+
+// Chunk length (a multiple of kChunkQuantum) such that rows x chunks about fills the
+// device with three compact CTAs per SM.
+int64_t chunk_len_for(int64_t row_stride, int32_t rows, int sms) {
+  int64_t want = (int64_t)(3 * (sms > 0 ? sms : 1)) / (rows > 0 ? rows : 1);
+  if (want < 1) want = 1;
+  int64_t len = (row_stride + want - 1) / want;
+  len = (len + kChunkQuantum - 1) / kChunkQuantum * kChunkQuantum;
+  return len;
+}
 
 }  // namespace
 
 size_t topk_long_workspace_bytes(int32_t rows, int64_t row_stride, int32_t k) {
   if (rows <= 0 || row_stride < 1 || k < 1) return 0;
-  return (size_t)rows * (size_t)row_bytes(chunks_of(row_stride), k, row_stride);
+  return (size_t)rows * (size_t)kRowBytes;
 }
 
 cudaError_t launch_topk_long(const float* logits, int64_t row_stride, int32_t rows,
                              const int32_t* row_starts, const int32_t* row_lens, int32_t k,
                              int32_t* idx, void* workspace, uint32_t* dev_status,
                              cudaStream_t stream) {
-  const int g = chunks_of(row_stride);
-  const int64_t blocks = (int64_t)rows * g;
+  int dev = 0, sms = 0;
+  cudaError_t ea = cudaGetDevice(&dev);
+  if (ea == cudaSuccess) ea = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ea != cudaSuccess) return ea;
+  const int64_t chunk_len = chunk_len_for(row_stride, rows, sms);
+  const int64_t g64 = (row_stride + chunk_len - 1) / chunk_len;
+  const int64_t blocks = (int64_t)rows * g64;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  const int g = (int)g64;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // Histograms, counters and chunk histograms start at zero (the rest needs no reset).
-  cudaError_t e = cudaMemset2DAsync(ws, (size_t)row_bytes(g, k, row_stride), 0,
-                                    (size_t)zeroed_bytes(g), (size_t)rows, stream);
+  // Each row's header (threshold, candidate count) starts at zero.
+  cudaError_t e = cudaMemset2DAsync(ws, (size_t)kRowBytes, 0, 16, (size_t)rows, stream);
   if (e != cudaSuccess) return e;
-  const size_t pick_smem = (size_t)k * sizeof(uint64_t);
-  topk_long_hist_kernel<false><<<(unsigned)blocks, kLThreads, 0, stream>>>(
-      logits, row_stride, row_starts, row_lens, k, g, 0, ws, dev_status);
+  topk_long_compact_kernel<<<(unsigned)blocks, kLThreads, 0, stream>>>(
+      logits, row_stride, row_starts, row_lens, k, g, chunk_len, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  topk_long_compact_kernel<<<(unsigned)blocks, kLThreads, pick_smem, stream>>>(
-      logits, row_stride, row_starts, row_lens, k, g, ws, dev_status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  for (int pass = 1; pass < kPasses; ++pass) {
-    topk_long_hist_kernel<true><<<(unsigned)blocks, kLThreads, 0, stream>>>(
-        logits, row_stride, row_starts, row_lens, k, g, pass, ws, dev_status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  topk_long_collect_kernel<<<(unsigned)blocks, kLThreads, pick_smem, stream>>>(
-      logits, row_stride, row_starts, row_lens, k, g, ws, dev_status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  int sort_n = 2;
-  while (sort_n < k) sort_n <<= 1;
-  const size_t smem = (size_t)sort_n * sizeof(uint64_t);
-  e = cudaFuncSetAttribute(topk_long_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = (size_t)(kCap + kMaxTake) * sizeof(uint64_t);
+  e = cudaFuncSetAttribute(topk_long_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e != cudaSuccess) return e;
-  topk_long_sort_kernel<<<rows, kSortThreads, smem, stream>>>(row_stride, row_starts, row_lens, k,
-                                                            g, sort_n, ws, idx);
+  topk_long_finish_kernel<<<rows, kFinishThreads, smem, stream>>>(
+      logits, row_stride, row_starts, row_lens, k, ws, idx, dev_status);
   return cudaGetLastError();
 }
 
