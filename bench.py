@@ -51,6 +51,9 @@ WORKLOAD = "hot-path step: vision attn (8547 tok, 16h, d80) + varlen causal GQA 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS = {"vision": "attn_fwd_kernel<80>", "varlen": "attn_fwd_kernel<128>",
            "topk": "topk_select_kernel", "sparse": "sparse_attn_kernel"}
+# this library's kernel launches per call of each part (the sparse call: the sort launch,
+# then the attention launch)
+LAUNCHES = {"vision": 1, "varlen": 1, "topk": 1, "sparse": 2}
 KERNEL_SOURCES = {"vision": "attn_fwd.cu", "varlen": "attn_fwd.cu", "topk": "topk.cu",
                   "sparse": "sparse_attn.cu", "vision_qkv_rope": "qkv_rope.cu",
                   "varlen_fp8": "attn_fwd.cu"}
@@ -250,11 +253,13 @@ class Step:
         self.o_sp = torch.empty((nq_here, self.sp.q.shape[1], self.sp.dv), **f32)
         self.l_sp = torch.empty((nq_here, self.sp.q.shape[1]), **f32)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        # attention workspace (work-item counter), shared by the two stream-ordered calls
-        ws = max(tts.attn_workspace_bytes(d[0].shape[0], d[1].shape[0], d[0].shape[1],
-                                          d[1].shape[1], d[0].shape[2], torch.bfloat16)
-                 for d in (self.d_vis, self.d_var))
-        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # attention workspaces (each call's work-item counter): one per call, since the
+        # step may run the two calls at the same time on different streams
+        def attn_ws(d):
+            n = tts.attn_workspace_bytes(d[0].shape[0], d[1].shape[0], d[0].shape[1],
+                                         d[1].shape[1], d[0].shape[2], torch.bfloat16)
+            return torch.empty(n, dtype=torch.uint8, device=dev)
+        self.ws_vis, self.ws_var = attn_ws(self.d_vis), attn_ws(self.d_var)
         # sparse workspace: partial results of the split last wave
         self.ws_sp = torch.empty(max(16, tts.sparse_workspace_bytes(nq_here)),
                                  dtype=torch.uint8, device=dev)
@@ -270,12 +275,12 @@ class Step:
         if name == "vision":
             q, k, v, cq, ck = self.d_vis
             t.attn_fwd_varlen(q, k, v, cq, ck, *self.mq["vision"], False, self.vis.scale,
-                              out=self.o_vis, lse=self.l_vis, workspace=self.ws,
+                              out=self.o_vis, lse=self.l_vis, workspace=self.ws_vis,
                               status=self.status)
         elif name == "varlen":
             q, k, v, cq, ck = self.d_var
             t.attn_fwd_varlen(q, k, v, cq, ck, *self.mq["varlen"], True, self.var.scale,
-                              out=self.o_var, lse=self.l_var, workspace=self.ws,
+                              out=self.o_var, lse=self.l_var, workspace=self.ws_var,
                               status=self.status)
         elif name == "topk":
             lg, rs, rl = self.d_tk
@@ -331,7 +336,7 @@ class Step:
                 def run(t0=t0, t1=t1, cuc=cuc, mq=mq):
                     t.attn_fwd_varlen(q[t0:t1], k[t0:t1], v[t0:t1], cuc, cuc, mq, mq, True,
                                       self.var.scale, out=self.o_var[t0:t1],
-                                      lse=self.l_var[t0:t1], workspace=self.ws,
+                                      lse=self.l_var[t0:t1], workspace=self.ws_var,
                                       status=self.status)
                 units.append((f"varlen[{a}:{b}]", ins, outs, run))
         if "vision" in parts:
@@ -569,7 +574,7 @@ def fp8_prefill_protocol(step, dev, peaks, flush):
             ev[2].record(s)
             t.attn_fwd_varlen_fp8(q8, qs, k8, ks, v, cq, ck, var.max_seqlen_q,
                                   var.max_seqlen_k, True, var.scale, out=out, lse=lse,
-                                  workspace=step.ws, status=step.status)
+                                  workspace=step.ws_var, status=step.status)
             ev[3].record(s)
             ev[3].synchronize()
             if it >= 4:
@@ -742,6 +747,7 @@ def run_gpu(args, rank, world, local):
             dist.all_gather_into_tensor(recv, send)
 
     def one_step(ev=None):
+        """The parts one after another on one stream (events between them time each)."""
         for i, p in enumerate(parts):
             if ev is not None:
                 ev[i].record(stream)
@@ -751,13 +757,40 @@ def run_gpu(args, rank, world, local):
         if ev is not None:
             ev[len(parts)].record(stream)
 
+    # The step's parts are independent (no part reads another's results), so the step
+    # issues each on a stream of its own, the vision call first: the CTAs of the next
+    # call take the SMs that a call's last, partial wave leaves idle.
+    order = [p for p in ("vision", "varlen", "sparse", "topk") if p in parts]
+    part_streams = {p: torch.cuda.Stream(dev) for p in order}
+    ev_fork = torch.cuda.Event()
+    ev_join = {p: torch.cuda.Event() for p in order}
+
+    def concurrent_step(e0=None, e1=None):
+        if e0 is not None:
+            e0.record(stream)
+        ev_fork.record(stream)
+        for p in order:
+            ps = part_streams[p]
+            ps.wait_event(ev_fork)
+            with torch.cuda.stream(ps):
+                step.part(p)
+            ev_join[p].record(ps)
+        for p in order:
+            stream.wait_event(ev_join[p])
+        if gather is not None:
+            gather()
+        if e1 is not None:
+            e1.record(stream)
+
+    timed_step = one_step if args.serial else concurrent_step
     for _ in range(max(3, args.warmup)):
         one_step()
+        concurrent_step()
     torch.cuda.synchronize()
     tts.check_status(step.status, "bench warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
-           for _ in range(args.steps)]
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -766,18 +799,34 @@ def run_gpu(args, rank, world, local):
         t_wall0 = time.perf_counter()
         for k in range(args.steps):
             flush.zero_()  # L2 flush between timed steps (outside the step's events)
-            one_step(evs[k])
+            if args.serial:
+                ev_step[k][0].record(stream)
+                one_step()
+                ev_step[k][1].record(stream)
+            else:
+                concurrent_step(*ev_step[k])
         torch.cuda.synchronize()
         t_wall1 = time.perf_counter()
         barrier(world)
     tts.check_status(step.status, "bench timed region")
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    # Per-part figures: the same steps with the parts one after another on one stream.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        one_step(evs[k])
+    torch.cuda.synchronize()
+    tts.check_status(step.status, "bench per-part pass")
     per_part = {p: [] for p in parts}
-    step_ms = []
+    serial_ms = []
     for k in range(args.steps):
         e = evs[k]
         for i, p in enumerate(parts):
             per_part[p].append(e[i].elapsed_time(e[i + 1]))
-        step_ms.append(e[0].elapsed_time(e[len(parts)]))
+        serial_ms.append(e[0].elapsed_time(e[len(parts)]))
+    del timed_step
     ms_step_local = float(np.mean(step_ms))
     ms_step = max_over_ranks(ms_step_local, world)
     attn_flops = sum(step.flops[p] for p in parts if p in step.flops)
@@ -793,7 +842,7 @@ def run_gpu(args, rank, world, local):
     comp = {}
     for p in parts:
         ms = float(np.mean(per_part[p]))
-        c = {"ms": ms, "kernel": KERNELS[p], "launches_per_step": 1}
+        c = {"ms": ms, "kernel": KERNELS[p], "launches_per_step": LAUNCHES[p]}
         if p in ("vision", "varlen"):
             tf = step.flops[p] / (ms * 1e-3) / 1e12
             c.update({"tflops": tf, "frac_bf16_peak": tf / tensor_peak})
@@ -905,11 +954,18 @@ def run_gpu(args, rank, world, local):
                                    "by queries" + (", results all-gathered" if gather else ""))
                    if args.shard else (f"replicas x{world}" if world > 1 else "single GPU"),
                    "shard_plan_rank0": step.plan, "lengths_varlen": step.var.lengths_q,
+                   "schedule": ("the parts one after another on one stream" if args.serial
+                                else "each part on a stream of its own (vision, varlen, sparse, "
+                                     "top-k issued in that order; the parts are independent), "
+                                     "so a part's last partial wave shares the GPU with the "
+                                     "next part's first CTAs; per-part figures from a pass with "
+                                     "the parts one after another"),
+                   "ms_per_step_parts_in_sequence": float(np.mean(serial_ms)),
                    "l2": "flushed between steps (256 MB write outside the step's events); "
                          "step inputs also exceed L2",
                    "ms_wall_timed_region": (t_wall1 - t_wall0) * 1e3},
         "components": comp, "roofline": roof, "cpu_baseline": cpu_base, "e2e": e2e,
-        "gpu_launches": len(parts) * args.steps, "clocks": clocks,
+        "gpu_launches": sum(LAUNCHES[p] for p in parts) * args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
 
@@ -928,6 +984,8 @@ def main():
                          "running one whole step per rank (weak scaling, the default)")
     ap.add_argument("--gather", action="store_true",
                     help="with --shard: all-gather every rank's results inside the step")
+    ap.add_argument("--serial", action="store_true",
+                    help="time the step with its parts one after another on one stream")
     ap.add_argument("--small", action="store_true",
                     help="profiling-sized varlen batch (4 sequences, 10096 tokens)")
     args = ap.parse_args()
