@@ -232,8 +232,11 @@ __device__ __forceinline__ uint32_t half16(uint32_t word, uint32_t b) {
   return (word >> ((b & 1u) * 16u)) & 0xFFFFu;
 }
 
+// have_pre: pre holds the window's values already loaded by this thread (element st at
+// pre[st]), as the kernel does for windows that start at the row's beginning.
 __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n, int k,
-                                            int32_t* __restrict__ out, uint8_t* smem) {
+                                            int32_t* __restrict__ out, uint8_t* smem,
+                                            const float (&pre)[kSortPerThread], bool have_pre) {
   uint32_t* const start = reinterpret_cast<uint32_t*>(smem);                  // [kBuckets/2]
   uint32_t* const cur = reinterpret_cast<uint32_t*>(smem + 2 * kBuckets);     // [kBuckets/2]
   uint32_t* const comp = reinterpret_cast<uint32_t*>(smem + 4 * kBuckets);    // [kSortMax]
@@ -259,7 +262,7 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
     const int i = st * kTopkThreads + tid;
     sk[st] = 0u;
     if (i < n) {
-      uint32_t u = __float_as_uint(__ldg(src + i));
+      uint32_t u = __float_as_uint(have_pre ? pre[st] : __ldg(src + i));
       if ((u & 0x7FFFFFFFu) == 0) u = 0;
       const uint32_t s = (u & 0x80000000u) ? u : ~(u | 0x80000000u);  // ~ordered_key
       sk[st] = s;
@@ -404,6 +407,15 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
   const int tid = threadIdx.x;
   const int64_t r = blockIdx.x;
   int32_t* out = idx + r * (int64_t)k;
+  // Windows usually start at the row's beginning: the row's first values are loaded
+  // while its bounds are read, saving a dependent round trip (used only if st == 0).
+  float pre[kSortPerThread];
+  const int64_t pre_n = row_stride < kSortMax ? row_stride : kSortMax;
+#pragma unroll
+  for (int e = 0; e < kSortPerThread; ++e) {
+    const int i = e * kTopkThreads + tid;
+    pre[e] = (i < pre_n) ? __ldg(logits + r * row_stride + i) : 0.f;
+  }
   const int64_t st = row_starts[r];
   const int64_t len = row_lens[r];
   if (st < 0 || len < 0 || st + len > row_stride) {
@@ -414,7 +426,7 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
   const int n = static_cast<int>(len);
   const float* src = logits + r * row_stride + st;
   if (n <= kSortMax) {
-    if (!bucket_topk(src, n, k, out, smem)) {
+    if (!bucket_topk(src, n, k, out, smem, pre, st == 0)) {
       __syncthreads();  // the radix path reuses the shared memory
       radix_topk(src, n, k, out, smem);
     }
