@@ -46,6 +46,7 @@ constexpr int kUnroll = 8;            // loads in flight per thread (scalar path
 constexpr int kUnroll4 = 4;           // float4 loads in flight per thread (vector path)
 constexpr int kSampleBlocks = 128;    // 32-value sample blocks per row, at most
 constexpr int kSampleBits = 12;       // key bits of the sample histogram
+static_assert(kSampleBlocks * 32 % 512 == 0, "whole rounds of samples per thread");
 constexpr int kFinishThreads = 1024;
 constexpr int kMaxTake = 4096;        // k <= 4096
 constexpr int kFWarps = kFinishThreads / 32;
@@ -115,12 +116,18 @@ __device__ uint32_t sample_threshold(const float* __restrict__ x, int64_t len, i
   for (int b = threadIdx.x; b < (1 << kSampleBits); b += kLThreads) hist[b] = 0u;
   if (threadIdx.x == 0) *s_t = 0u;  // sample too small to reach `want`: every key
   __syncthreads();
-  // ns is a multiple of 32, so every lane of a warp takes the same number of steps.
-  for (int64_t s = threadIdx.x; s < ns; s += kLThreads) {
-    const int64_t j = (s >> 5) * stride + (s & 31);
-    const uint32_t b = key_of(__ldg(x + j)) >> (32 - kSampleBits);
-    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);  // one atomic per bucket
-    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[b], (uint32_t)__popc(peers));
+  // Every sample load goes out before any is used (one round trip, not one per sample).
+  constexpr int kPerThread = kSampleBlocks * 32 / kLThreads;
+  float sv[kPerThread];
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int64_t s = (int64_t)u * kLThreads + threadIdx.x;
+    sv[u] = (s < ns) ? __ldg(x + (s >> 5) * stride + (s & 31)) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int64_t s = (int64_t)u * kLThreads + threadIdx.x;
+    if (s < ns) atomicAdd(&hist[key_of(sv[u]) >> (32 - kSampleBits)], 1u);
   }
   __syncthreads();
   // Descending walk: thread t owns buckets 4095 - 8t down to 4088 - 8t.
@@ -232,23 +239,73 @@ __global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
 }
 
 // ---------------------------------------------------------------------------- 3. finish
-// Bitonic sort of sel[0, n) descending (n a power of two), by the whole block.
-__device__ __forceinline__ void sort_desc(uint64_t* sel, int n) {
+// Bitonic sort, descending, of the n = E * kFinishThreads composites in buf (E = 2 or 4),
+// whose result it writes to out as positions (the first `take`, then -1 up to k). Thread
+// t holds elements t E .. t E + E - 1 in registers. Compare-exchanges between elements of
+// one thread are register swaps, between threads of one warp shuffles; only strides of
+// 32 E or more go through shared memory (double-buffered in buf and spare: one barrier
+// per such stage). The network is the textbook one: for size = 2, 4, .., n and stride =
+// size / 2, .., 1, the element e and its partner e ^ stride are put in descending order
+// when e & size is 0 and in ascending order otherwise.
+template <int E>
+__device__ void sort_desc_out(uint64_t* buf, uint64_t* spare, int take, int k,
+                              int32_t* __restrict__ out) {
+  constexpr int n = E * kFinishThreads;
+  const int lane = threadIdx.x & 31;
+  const int e0 = threadIdx.x * E;
+  uint64_t v[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) v[i] = buf[e0 + i];
+  uint64_t* bufs[2] = {spare, buf};
+  int which = 0;
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (n >> 1); i += kFinishThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t a = sel[lo], b = sel[hi];
-        if ((a < b) == desc) {
-          sel[lo] = b;
-          sel[hi] = a;
+      if (stride >= 32 * E) {  // partner in another warp: through shared memory
+        uint64_t* b = bufs[which];
+        which ^= 1;
+#pragma unroll
+        for (int i = 0; i < E; ++i) b[e0 + i] = v[i];
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const int e = e0 + i;
+          const uint64_t p = b[e ^ stride];
+          const bool desc = (e & size) == 0, lo = (e & stride) == 0;
+          v[i] = (desc == lo) ? (v[i] > p ? v[i] : p) : (v[i] < p ? v[i] : p);
+        }
+      } else if (stride >= E) {  // partner in another lane of this warp
+        const int lm = stride / E;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const int e = e0 + i;
+          const uint64_t p = __shfl_xor_sync(0xFFFFFFFFu, v[i], lm);
+          const bool desc = (e & size) == 0, lo = (e & stride) == 0;
+          v[i] = (desc == lo) ? (v[i] > p ? v[i] : p) : (v[i] < p ? v[i] : p);
+        }
+      } else {  // partner in this thread
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const bool desc = ((e0 + i) & size) == 0;
+            const uint64_t a = v[i], c = v[j];
+            if ((a < c) == desc) {
+              v[i] = c;
+              v[j] = a;
+            }
+          }
         }
       }
-      __syncthreads();
     }
   }
+  (void)lane;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int e = e0 + i;
+    if (e < k)
+      out[e] = (e < take) ? static_cast<int32_t>(~static_cast<uint32_t>(v[i] & 0xFFFFFFFFull)) : -1;
+  }
+  for (int e = n + threadIdx.x; e < k; e += kFinishThreads) out[e] = -1;
 }
 
 // Exact selection by one CTA straight from the window: MSB-first radix select (4 x 8
@@ -326,6 +383,7 @@ __global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
   __shared__ int hist[256];
   __shared__ int warp_tot[kFWarps];
   __shared__ int s_digit, s_above, s_n;
+  __shared__ unsigned long long s_or, s_and;
   const int64_t row = blockIdx.x;
   const int64_t st = row_starts[row], len = row_lens[row];
   int32_t* out = idx + row * (int64_t)k;
@@ -340,14 +398,42 @@ __global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
   if (cnt >= take && cnt <= kCap) {
     const int n = (int)cnt;
     const uint64_t* cand = row_cand(ws, row);
-    for (int j = threadIdx.x; j < n; j += kFinishThreads) sel[j] = __ldcg(cand + j);
+    // Load, with a census of the bits (OR / AND) so that bytes on which every candidate
+    // agrees need no pass below.
+    unsigned long long c_or = 0ull, c_and = ~0ull;
+    for (int j = threadIdx.x; j < n; j += kFinishThreads) {
+      const uint64_t c = __ldcg(cand + j);
+      sel[j] = c;
+      c_or |= c;
+      c_and &= c;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      c_or |= __shfl_xor_sync(0xFFFFFFFFu, c_or, o);
+      c_and &= __shfl_xor_sync(0xFFFFFFFFu, c_and, o);
+    }
+    if (threadIdx.x == 0) {
+      s_or = 0ull;
+      s_and = ~0ull;
+    }
     __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+      atomicOr(&s_or, c_or);
+      atomicAnd(&s_and, c_and);
+    }
+    __syncthreads();
+    const uint64_t varying = s_or ^ s_and, common = s_and;
     // The take-th largest composite C among the candidates (they are unique): an
     // MSB-first radix select over the 64 bits, then every composite >= C is a pick.
     uint64_t prefix = 0, mask = 0;
     int remaining = take;
     for (int pass = 0; pass < 8 && n > take; ++pass) {
       const int shift = 56 - 8 * pass;
+      if (((varying >> shift) & 0xFFu) == 0) {  // the same byte in every candidate
+        prefix |= common & (0xFFull << shift);
+        mask |= 0xFFull << shift;
+        continue;
+      }
       for (int b = threadIdx.x; b < 256; b += kFinishThreads) hist[b] = 0;
       __syncthreads();
       for (int j = threadIdx.x; j < n; j += kFinishThreads) {
@@ -399,15 +485,14 @@ __global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
     select_exact(logits + row * row_stride + st, len, take, picks, hist, warp_tot, &s_digit,
                  &s_above, &s_n);
   }
-  int sort_n = 1;
-  while (sort_n < take) sort_n <<= 1;
-  for (int j = take + threadIdx.x; j < sort_n; j += kFinishThreads) picks[j] = 0ull;  // last
+  // Sort the picks (padding with 0, which sorts last) and write their positions.
+  const int sort_n = take <= 2 * kFinishThreads ? 2 * kFinishThreads : 4 * kFinishThreads;
+  for (int j = take + threadIdx.x; j < sort_n; j += kFinishThreads) picks[j] = 0ull;
   __syncthreads();
-  sort_desc(picks, sort_n);
-  uint64_t* const sel_out = picks;
-  for (int j = threadIdx.x; j < k; j += kFinishThreads)
-    out[j] = (j < take) ? static_cast<int32_t>(~static_cast<uint32_t>(sel_out[j] & 0xFFFFFFFFull))
-                        : -1;
+  if (sort_n == 2 * kFinishThreads)
+    sort_desc_out<2>(picks, sel, take, k, out);
+  else
+    sort_desc_out<4>(picks, sel, take, k, out);
 }
 
 // Chunk length (a multiple of kChunkQuantum) such that rows x chunks about fills the
