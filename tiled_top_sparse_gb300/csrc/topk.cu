@@ -207,10 +207,11 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
 // -0 folded onto +0). The keys of each sign half (skey < 2^31: values >= +0; skey >= 2^31:
 // negative values) are mapped linearly onto kHalfBuckets buckets between the half's
 // smallest and largest key, so bucket order is key order, and a counting pass places
-// every bucket at its final offset. Inside a bucket the elements are ranked by the
-// unique composite (key offset inside the bucket << 12 | position), which orders
-// exactly as (value descending, position ascending); a bucket spans at most 2^19 key
-// codes (a half's span is below 2^31, divided into 2^12 buckets) and positions need
+// every bucket at its final offset. The counting pass's atomic also hands each element a
+// slot inside its bucket (in no particular order). Inside a bucket the elements are
+// ranked by the unique composite (key offset inside the bucket << 12 | position), which
+// orders exactly as (value descending, position ascending); a bucket spans at most 2^19
+// key codes (a half's span is below 2^31, divided into 2^12 buckets) and positions need
 // 12 bits, so the composite fits 31 bits. The rank of an element is the number of
 // smaller composites in its bucket, found by comparing against every member: cheap
 // while buckets hold a handful of values, which is the case unless the window's values
@@ -222,28 +223,19 @@ constexpr int kHalfBits = 11;
 constexpr int kHalfBuckets = 1 << kHalfBits;
 constexpr int kBuckets = 2 * kHalfBuckets;
 constexpr uint32_t kMaxBucket = 128;
-static_assert(kBuckets == 8 * kTopkThreads, "the scan gives every thread one uint4 of counters");
+static_assert(kBuckets == 8 * kTopkThreads, "the scan gives every thread two uint4 of counters");
 static_assert(kSortMax <= 4096, "positions must fit the composite's 12 bits");
-// Shared memory: bucket starts (16-bit counters, two to a word), insertion cursors,
-// the bucketed composites with their bucket ids, and the staged output.
-constexpr size_t kBucketSmem = 2 * (kBuckets / 2) * 4 + kSortMax * (4 + 2 + 4);
-
-__device__ __forceinline__ uint32_t half16(uint32_t word, uint32_t b) {
-  return (word >> ((b & 1u) * 16u)) & 0xFFFFu;
-}
+// Shared memory: one word per bucket (its count, then its start | end << 16), and per
+// selectable slot the composite with its bucket's word.
+constexpr size_t kBucketSmem = 4 * kBuckets + 8 * kSortMax;
 
 // have_pre: pre holds the window's values already loaded by this thread (element st at
 // pre[st]), as the kernel does for windows that start at the row's beginning.
 __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n, int k,
                                             int32_t* __restrict__ out, uint8_t* smem,
                                             const float (&pre)[kSortPerThread], bool have_pre) {
-  uint32_t* const start = reinterpret_cast<uint32_t*>(smem);                  // [kBuckets/2]
-  uint32_t* const cur = reinterpret_cast<uint32_t*>(smem + 2 * kBuckets);     // [kBuckets/2]
-  uint32_t* const comp = reinterpret_cast<uint32_t*>(smem + 4 * kBuckets);    // [kSortMax]
-  uint16_t* const bid =
-      reinterpret_cast<uint16_t*>(smem + 4 * kBuckets + 4 * kSortMax);        // [kSortMax]
-  int32_t* const staged =
-      reinterpret_cast<int32_t*>(smem + 4 * kBuckets + 6 * kSortMax);         // [kSortMax]
+  uint32_t* const se = reinterpret_cast<uint32_t*>(smem);              // [kBuckets]
+  uint2* const slots = reinterpret_cast<uint2*>(smem + 4 * kBuckets);  // [kSortMax]
   __shared__ uint32_t s_rng[4];  // min / max skey of the non-negative half, then the negative
   __shared__ uint32_t s_maxc, s_ranked;
   __shared__ uint32_t s_wsum[kWarps];
@@ -253,12 +245,15 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
     s_maxc = 0u;
     s_ranked = static_cast<uint32_t>(n);
   }
-  reinterpret_cast<uint4*>(start)[tid] = make_uint4(0u, 0u, 0u, 0u);
-  // Element st of thread tid is window position st * kTopkThreads + tid (coalesced).
+  reinterpret_cast<uint4*>(se)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
+  reinterpret_cast<uint4*>(se)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+  // Element st of thread tid is window position st * kTopkThreads + tid (coalesced). A
+  // warp whose first position of step st lies past the window stops there (warp-uniform).
   uint32_t sk[kSortPerThread];
   uint32_t pmin = 0xFFFFFFFFu, pmax = 0u, nmin = 0xFFFFFFFFu, nmax = 0u;
 #pragma unroll
   for (int st = 0; st < kSortPerThread; ++st) {
+    if (st * kTopkThreads + warp * 32 >= n) break;
     const int i = st * kTopkThreads + tid;
     sk[st] = 0u;
     if (i < n) {
@@ -294,35 +289,37 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
   const uint32_t span0 = s_rng[1] - base0, span1 = s_rng[3] - base1;  // garbage if empty
   const int sh0 = max(0, (32 - __clz(span0)) - kHalfBits);
   const int sh1 = max(0, (32 - __clz(span1)) - kHalfBits);
-  uint32_t bkt[kSortPerThread];
+  // Per element: bucket << 16 | its slot inside the bucket (the count before it), or ~0.
+  uint32_t bs[kSortPerThread];
 #pragma unroll
   for (int st = 0; st < kSortPerThread; ++st) {
+    if (st * kTopkThreads + warp * 32 >= n) break;
     const int i = st * kTopkThreads + tid;
-    bkt[st] = 0xFFFFFFFFu;
+    bs[st] = 0xFFFFFFFFu;
     if (i < n) {
       const uint32_t s = sk[st];
       const bool neg = s >= 0x80000000u;
       const uint32_t off = s - (neg ? base1 : base0);
       const int sh = neg ? sh1 : sh0;
-      bkt[st] = (neg ? kHalfBuckets : 0) + (off >> sh);
+      const uint32_t b = (neg ? kHalfBuckets : 0) + (off >> sh);
       sk[st] = ((off & ((1u << sh) - 1u)) << 12) | static_cast<uint32_t>(i);  // composite
-      atomicAdd(&start[bkt[st] >> 1], 1u << ((bkt[st] & 1u) * 16u));
+      bs[st] = (b << 16) | atomicAdd(&se[b], 1u);
     }
   }
   __syncthreads();
   // Exclusive prefix over the buckets in ascending order: thread tid owns buckets
-  // [8 tid, 8 tid + 8), one uint4 of counters. Counts and starts stay below 2^16. The
-  // thread whose bucket holds output place k - 1 records where that bucket ends: every
-  // slot before it is ranked, nothing after it is selected.
+  // [8 tid, 8 tid + 8). Counts and offsets stay below 2^16. Each bucket's word becomes
+  // start | end << 16. The thread whose bucket holds output place k - 1 records where
+  // that bucket ends: every slot before it is ranked, nothing after it is selected.
   {
-    const uint4 c = reinterpret_cast<uint4*>(start)[tid];
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    const uint4 c0 = reinterpret_cast<const uint4*>(se)[2 * tid];
+    const uint4 c1 = reinterpret_cast<const uint4*>(se)[2 * tid + 1];
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     uint32_t tot = 0u, mx = 0u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t lo = w[j] & 0xFFFFu, hi = w[j] >> 16;
-      tot += lo + hi;
-      mx = max(mx, max(lo, hi));
+    for (int j = 0; j < 8; ++j) {
+      tot += w[j];
+      mx = max(mx, w[j]);
     }
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
     uint32_t x = tot;
@@ -342,53 +339,46 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
       run += (4 * q + 0 < warp ? v.x : 0u) + (4 * q + 1 < warp ? v.y : 0u) +
              (4 * q + 2 < warp ? v.z : 0u) + (4 * q + 3 < warp ? v.w : 0u);
     }
-    uint32_t o[4];
+    uint32_t o[8];
     const uint32_t kk = static_cast<uint32_t>(k);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t lo = w[j] & 0xFFFFu, hi = w[j] >> 16;
-      o[j] = run | ((run + lo) << 16);
-      if (run < kk && kk <= run + lo) s_ranked = run + lo;
-      if (run + lo < kk && kk <= run + lo + hi) s_ranked = run + lo + hi;
-      run += lo + hi;
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t e = run + w[j];
+      o[j] = run | (e << 16);
+      if (run < kk && kk <= e) s_ranked = e;
+      run = e;
     }
-    const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-    reinterpret_cast<uint4*>(start)[tid] = ov;
-    reinterpret_cast<uint4*>(cur)[tid] = ov;
+    reinterpret_cast<uint4*>(se)[2 * tid] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(se)[2 * tid + 1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
   __syncthreads();
   if (s_maxc > kMaxBucket) return false;  // uniform: every thread reads the same word
   const uint32_t ranked = s_ranked;        // slots [0, ranked) hold the selectable buckets
-  // Scatter the composites of buckets that start before k (and their bucket ids).
+  // Place the composites of buckets that start before k, each with its bucket's word.
 #pragma unroll
   for (int st = 0; st < kSortPerThread; ++st) {
-    const uint32_t b = bkt[st];
-    if (b != 0xFFFFFFFFu && half16(start[b >> 1], b) < static_cast<uint32_t>(k)) {
-      const uint32_t old = atomicAdd(&cur[b >> 1], 1u << ((b & 1u) * 16u));
-      const uint32_t slot = half16(old, b);
-      comp[slot] = sk[st];
-      bid[slot] = static_cast<uint16_t>(b);
+    if (st * kTopkThreads + warp * 32 >= n) break;
+    const uint32_t v = bs[st];
+    if (v != 0xFFFFFFFFu) {
+      const uint32_t bw = se[v >> 16];
+      const uint32_t s0 = bw & 0xFFFFu;
+      if (s0 < static_cast<uint32_t>(k)) slots[s0 + (v & 0xFFFFu)] = make_uint2(sk[st], bw);
     }
   }
   __syncthreads();
   // Rank in bucket order: thread tid takes slots tid, tid + 512, ...; neighbouring lanes
   // hold neighbouring slots, mostly of the same bucket, so their loads of the bucket's
-  // members coincide. The rank of a slot is the number of smaller composites in its
-  // bucket; its place is the bucket's start plus that rank.
+  // members coincide, and their places (the bucket's start plus the number of smaller
+  // composites in it) fall in the same few output lines.
   for (uint32_t j = tid; j < ranked; j += kTopkThreads) {
-    const uint32_t me = comp[j];
-    const uint32_t b = bid[j];
-    const uint32_t s0 = half16(start[b >> 1], b);
-    const uint32_t s1 = (b + 1 < kBuckets) ? half16(start[(b + 1) >> 1], b + 1)
-                                           : static_cast<uint32_t>(n);
+    const uint2 me = slots[j];
+    const uint32_t s0 = me.y & 0xFFFFu, s1 = me.y >> 16;
     uint32_t rank = 0;
-    for (uint32_t m = s0; m < s1; ++m) rank += comp[m] < me ? 1u : 0u;
+    for (uint32_t m = s0; m < s1; ++m) rank += slots[m].x < me.x ? 1u : 0u;
     const uint32_t dst = s0 + rank;
-    if (dst < static_cast<uint32_t>(k)) staged[dst] = static_cast<int32_t>(me & 0xFFFu);
+    if (dst < static_cast<uint32_t>(k)) out[dst] = static_cast<int32_t>(me.x & 0xFFFu);
   }
-  __syncthreads();
-  const int take = n < k ? n : k;
-  for (int j = tid; j < k; j += kTopkThreads) out[j] = (j < take) ? staged[j] : -1;
+  for (int j = n + tid; j < k; j += kTopkThreads) out[j] = -1;
   return true;
 }
 
