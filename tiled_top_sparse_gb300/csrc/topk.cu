@@ -229,11 +229,11 @@ static_assert(kSortMax <= 4096, "positions must fit the composite's 12 bits");
 // selectable slot the composite with its bucket's word.
 constexpr size_t kBucketSmem = 4 * kBuckets + 8 * kSortMax;
 
-// have_pre: pre holds the window's values already loaded by this thread (element st at
-// pre[st]), as the kernel does for windows that start at the row's beginning.
-__device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n, int k,
-                                            int32_t* __restrict__ out, uint8_t* smem,
-                                            const float (&pre)[kSortPerThread], bool have_pre) {
+// value(st, i) gives element st of this thread (window position i = st * kTopkThreads +
+// tid).
+template <class Value>
+__device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* __restrict__ out,
+                                            uint8_t* smem) {
   uint32_t* const se = reinterpret_cast<uint32_t*>(smem);              // [kBuckets]
   uint2* const slots = reinterpret_cast<uint2*>(smem + 4 * kBuckets);  // [kSortMax]
   __shared__ uint32_t s_rng[4];  // min / max skey of the non-negative half, then the negative
@@ -257,7 +257,7 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
     const int i = st * kTopkThreads + tid;
     sk[st] = 0u;
     if (i < n) {
-      uint32_t u = __float_as_uint(have_pre ? pre[st] : __ldg(src + i));
+      uint32_t u = __float_as_uint(value(st, i));
       if ((u & 0x7FFFFFFFu) == 0) u = 0;
       const uint32_t s = (u & 0x80000000u) ? u : ~(u | 0x80000000u);  // ~ordered_key
       sk[st] = s;
@@ -289,6 +289,7 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
   const uint32_t span0 = s_rng[1] - base0, span1 = s_rng[3] - base1;  // garbage if empty
   const int sh0 = max(0, (32 - __clz(span0)) - kHalfBits);
   const int sh1 = max(0, (32 - __clz(span1)) - kHalfBits);
+  const uint32_t low0 = (1u << sh0) - 1u, low1 = (1u << sh1) - 1u;
   // Per element: bucket << 16 | its slot inside the bucket (the count before it), or ~0.
   uint32_t bs[kSortPerThread];
 #pragma unroll
@@ -302,7 +303,7 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
       const uint32_t off = s - (neg ? base1 : base0);
       const int sh = neg ? sh1 : sh0;
       const uint32_t b = (neg ? kHalfBuckets : 0) + (off >> sh);
-      sk[st] = ((off & ((1u << sh) - 1u)) << 12) | static_cast<uint32_t>(i);  // composite
+      sk[st] = ((off & (neg ? low1 : low0)) << 12) | static_cast<uint32_t>(i);  // composite
       bs[st] = (b << 16) | atomicAdd(&se[b], 1u);
     }
   }
@@ -331,21 +332,15 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
     if (lane == 31) s_wsum[warp] = x;
     if (lane == 0) atomicMax(&s_maxc, mx);
     __syncthreads();
-    uint32_t run = x - tot;
-    const uint4* ws4 = reinterpret_cast<const uint4*>(s_wsum);
-#pragma unroll
-    for (int q = 0; q < kWarps / 4; ++q) {
-      const uint4 v = ws4[q];
-      run += (4 * q + 0 < warp ? v.x : 0u) + (4 * q + 1 < warp ? v.y : 0u) +
-             (4 * q + 2 < warp ? v.z : 0u) + (4 * q + 3 < warp ? v.w : 0u);
-    }
-    uint32_t o[8];
+    uint32_t run = x - tot + __reduce_add_sync(0xFFFFFFFFu, lane < warp ? s_wsum[lane] : 0u);
     const uint32_t kk = static_cast<uint32_t>(k);
+    const bool mine = run < kk && kk <= run + tot;  // place k - 1 lies in these buckets
+    uint32_t o[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t e = run + w[j];
       o[j] = run | (e << 16);
-      if (run < kk && kk <= e) s_ranked = e;
+      if (mine && run < kk && kk <= e) s_ranked = e;
       run = e;
     }
     reinterpret_cast<uint4*>(se)[2 * tid] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -372,9 +367,11 @@ __device__ __forceinline__ bool bucket_topk(const float* __restrict__ src, int n
   // composites in it) fall in the same few output lines.
   for (uint32_t j = tid; j < ranked; j += kTopkThreads) {
     const uint2 me = slots[j];
-    const uint32_t s0 = me.y & 0xFFFFu, s1 = me.y >> 16;
+    const uint32_t s0 = me.y & 0xFFFFu;
     uint32_t rank = 0;
-    for (uint32_t m = s0; m < s1; ++m) rank += slots[m].x < me.x ? 1u : 0u;
+    const uint2* const end = slots + (me.y >> 16);
+#pragma unroll 1  // buckets hold a few values: an unrolled loop costs more than it saves
+    for (const uint2* m = slots + s0; m < end; ++m) rank += m->x < me.x ? 1u : 0u;
     const uint32_t dst = s0 + rank;
     if (dst < static_cast<uint32_t>(k)) out[dst] = static_cast<int32_t>(me.x & 0xFFFu);
   }
@@ -400,11 +397,14 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
   // Windows usually start at the row's beginning: the row's first values are loaded
   // while its bounds are read, saving a dependent round trip (used only if st == 0).
   float pre[kSortPerThread];
-  const int64_t pre_n = row_stride < kSortMax ? row_stride : kSortMax;
+  const int pre_n = static_cast<int>(row_stride < kSortMax ? row_stride : kSortMax);
+  const float* row = logits + r * row_stride;
 #pragma unroll
   for (int e = 0; e < kSortPerThread; ++e) {
+    pre[e] = 0.f;
+    if (e * kTopkThreads + (tid & ~31) >= pre_n) continue;  // warp-uniform
     const int i = e * kTopkThreads + tid;
-    pre[e] = (i < pre_n) ? __ldg(logits + r * row_stride + i) : 0.f;
+    if (i < pre_n) pre[e] = __ldg(row + i);
   }
   const int64_t st = row_starts[r];
   const int64_t len = row_lens[r];
@@ -416,7 +416,9 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
   const int n = static_cast<int>(len);
   const float* src = logits + r * row_stride + st;
   if (n <= kSortMax) {
-    if (!bucket_topk(src, n, k, out, smem, pre, st == 0)) {
+    const bool have_pre = st == 0;
+    auto value = [&](int e, int i) { return have_pre ? pre[e] : __ldg(src + i); };
+    if (!bucket_topk(value, n, k, out, smem)) {
       __syncthreads();  // the radix path reuses the shared memory
       radix_topk(src, n, k, out, smem);
     }
