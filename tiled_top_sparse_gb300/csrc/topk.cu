@@ -35,10 +35,18 @@ namespace {
 
 constexpr int kTopkThreads = 512;
 constexpr int kWarps = kTopkThreads / 32;
-constexpr int kSortPerThread = 8;                          // values per thread, radix path
-constexpr int kSortMax = kTopkThreads * kSortPerThread;    // longest window it sorts
+// The one-CTA paths hold E values per thread, so they sort windows of up to
+// kTopkThreads * E values: E = 6 where rows are at most 3072 long (less shared memory:
+// four CTAs per SM), E = 8 up to 4096 (three).
+template <int E>
+constexpr int sort_max() {
+  return kTopkThreads * E;
+}
 // Shared memory of the radix path: two key/position buffers and per-warp digit counters.
-constexpr size_t kRadixSmem = 2 * kSortMax * (4 + 2) + kWarps * 256 * 4;
+template <int E>
+constexpr size_t radix_smem() {
+  return 2 * sort_max<E>() * (4 + 2) + kWarps * 256 * 4;
+}
 
 __device__ __forceinline__ uint32_t ordered_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -79,8 +87,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
 // Element order inside a pass: warp w owns indices [w * 32E, (w + 1) * 32E), step s
 // of lane l holds index w * 32E + 32 s + l, so ranks computed warp by warp and step
 // by step preserve the input order of equal digits.
+template <int P>
 __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n, int k,
                                           int32_t* __restrict__ out, uint8_t* smem) {
+  constexpr int kSortPerThread = P;
+  constexpr int kSortMax = sort_max<P>();
   uint32_t* const key_buf = reinterpret_cast<uint32_t*>(smem);              // [2][kSortMax]
   uint16_t* const pos_buf = reinterpret_cast<uint16_t*>(smem + 8 * kSortMax);  // [2][kSortMax]
   uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + 12 * kSortMax);  // [kWarps][256]
@@ -88,7 +99,7 @@ __device__ __forceinline__ void radix_topk(const float* __restrict__ src, int n,
   __shared__ int warp_tot[kWarps];
   __shared__ uint32_t s_or[2], s_and[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int E = (n + kTopkThreads - 1) / kTopkThreads;  // steps per warp (<= 8)
+  const int E = (n + kTopkThreads - 1) / kTopkThreads;  // steps per warp (<= P)
   const int wbase = warp * 32 * E;
   const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t* wcnt = cnt + warp * 256;
@@ -223,17 +234,23 @@ constexpr int kHalfBits = 11;
 constexpr int kHalfBuckets = 1 << kHalfBits;
 constexpr int kBuckets = 2 * kHalfBuckets;
 constexpr uint32_t kMaxBucket = 128;
-static_assert(kBuckets == 8 * kTopkThreads, "the scan gives every thread two uint4 of counters");
-static_assert(kSortMax <= 4096, "positions must fit the composite's 12 bits");
+constexpr int kThreadBuckets = kBuckets / kTopkThreads;  // buckets per thread in the scan
+static_assert(kThreadBuckets * kTopkThreads == kBuckets && kThreadBuckets % 4 == 0,
+              "the scan gives every thread whole uint4s of counters");
 // Shared memory: one word per bucket (its count, then its start | end << 16), and per
 // selectable slot the composite with its bucket's word.
-constexpr size_t kBucketSmem = 4 * kBuckets + 8 * kSortMax;
+template <int E>
+constexpr size_t bucket_smem() {
+  return 4 * kBuckets + 8 * sort_max<E>();
+}
 
 // value(st, i) gives element st of this thread (window position i = st * kTopkThreads +
 // tid).
-template <class Value>
+template <int E, class Value>
 __device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* __restrict__ out,
                                             uint8_t* smem) {
+  constexpr int kSortPerThread = E;
+  static_assert(sort_max<E>() <= 4096, "positions must fit the composite's 12 bits");
   uint32_t* const se = reinterpret_cast<uint32_t*>(smem);              // [kBuckets]
   uint2* const slots = reinterpret_cast<uint2*>(smem + 4 * kBuckets);  // [kSortMax]
   __shared__ uint32_t s_rng[4];  // min / max skey of the non-negative half, then the negative
@@ -245,8 +262,9 @@ __device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* 
     s_maxc = 0u;
     s_ranked = static_cast<uint32_t>(n);
   }
-  reinterpret_cast<uint4*>(se)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
-  reinterpret_cast<uint4*>(se)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int q = 0; q < kThreadBuckets / 4; ++q)
+    reinterpret_cast<uint4*>(se)[q * kTopkThreads + tid] = make_uint4(0u, 0u, 0u, 0u);
   // Element st of thread tid is window position st * kTopkThreads + tid (coalesced). A
   // warp whose first position of step st lies past the window stops there (warp-uniform).
   uint32_t sk[kSortPerThread];
@@ -309,16 +327,24 @@ __device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* 
   }
   __syncthreads();
   // Exclusive prefix over the buckets in ascending order: thread tid owns buckets
-  // [8 tid, 8 tid + 8). Counts and offsets stay below 2^16. Each bucket's word becomes
-  // start | end << 16. The thread whose bucket holds output place k - 1 records where
-  // that bucket ends: every slot before it is ranked, nothing after it is selected.
+  // [kThreadBuckets tid, kThreadBuckets (tid + 1)). Counts and offsets stay below 2^16.
+  // Each bucket's word becomes start | end << 16. The thread whose bucket holds output
+  // place k - 1 records where that bucket ends: every slot before it is ranked, nothing
+  // after it is selected.
   {
-    const uint4 c0 = reinterpret_cast<const uint4*>(se)[2 * tid];
-    const uint4 c1 = reinterpret_cast<const uint4*>(se)[2 * tid + 1];
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint4* const mine4 = reinterpret_cast<uint4*>(se) + tid * (kThreadBuckets / 4);
+    uint32_t w[kThreadBuckets];
+#pragma unroll
+    for (int q = 0; q < kThreadBuckets / 4; ++q) {
+      const uint4 c = mine4[q];
+      w[4 * q] = c.x;
+      w[4 * q + 1] = c.y;
+      w[4 * q + 2] = c.z;
+      w[4 * q + 3] = c.w;
+    }
     uint32_t tot = 0u, mx = 0u;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kThreadBuckets; ++j) {
       tot += w[j];
       mx = max(mx, w[j]);
     }
@@ -335,16 +361,17 @@ __device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* 
     uint32_t run = x - tot + __reduce_add_sync(0xFFFFFFFFu, lane < warp ? s_wsum[lane] : 0u);
     const uint32_t kk = static_cast<uint32_t>(k);
     const bool mine = run < kk && kk <= run + tot;  // place k - 1 lies in these buckets
-    uint32_t o[8];
+    uint32_t o[kThreadBuckets];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kThreadBuckets; ++j) {
       const uint32_t e = run + w[j];
       o[j] = run | (e << 16);
       if (mine && run < kk && kk <= e) s_ranked = e;
       run = e;
     }
-    reinterpret_cast<uint4*>(se)[2 * tid] = make_uint4(o[0], o[1], o[2], o[3]);
-    reinterpret_cast<uint4*>(se)[2 * tid + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int q = 0; q < kThreadBuckets / 4; ++q)
+      mine4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
   }
   __syncthreads();
   if (s_maxc > kMaxBucket) return false;  // uniform: every thread reads the same word
@@ -379,11 +406,14 @@ __device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* 
   return true;
 }
 
-// Three CTAs per SM (<= 40 registers a thread): 456 resident rows on 152 SMs.
-__global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
+// Four CTAs per SM for E = 6 (<= 32 registers a thread), three for E = 8 (<= 40).
+template <int E>
+__global__ void __launch_bounds__(kTopkThreads, E <= 6 ? 4 : 3) topk_select_kernel(
     const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
     const int32_t* __restrict__ row_lens, int k, int sort_n, int32_t* __restrict__ idx,
     uint32_t* dev_status) {
+  constexpr int kSortPerThread = E;
+  constexpr int kSortMax = sort_max<E>();
   extern __shared__ __align__(16) uint8_t smem[];
   uint64_t* sel = reinterpret_cast<uint64_t*>(smem);                      // [sort_n]
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + 8 * (size_t)sort_n);  // [row_stride]
@@ -418,9 +448,9 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
   if (n <= kSortMax) {
     const bool have_pre = st == 0;
     auto value = [&](int e, int i) { return have_pre ? pre[e] : __ldg(src + i); };
-    if (!bucket_topk(value, n, k, out, smem)) {
+    if (!bucket_topk<E>(value, n, k, out, smem)) {
       __syncthreads();  // the radix path reuses the shared memory
-      radix_topk(src, n, k, out, smem);
+      radix_topk<E>(src, n, k, out, smem);
     }
     return;
   }
@@ -531,24 +561,33 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_select_kernel(
 
 }  // namespace
 
-size_t topk_smem_bytes(int64_t row_stride, int k) {
+// Rows of at most sort_max<6>() values take the E = 6 kernel, all others E = 8.
+static bool short_rows(int64_t row_stride) { return row_stride <= sort_max<6>(); }
+
+template <int E>
+static size_t smem_bytes(int64_t row_stride, int k) {
   const int64_t cap = row_stride < k ? row_stride : k;
   int sort_n = 2;
   while (sort_n < cap) sort_n <<= 1;
-  const size_t sel = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
-  const size_t small = kRadixSmem > kBucketSmem ? kRadixSmem : kBucketSmem;
-  return sel < small ? small : sel;
+  size_t smem = 8 * (size_t)sort_n + 4 * (size_t)row_stride;  // the select path
+  if (row_stride <= sort_max<E>()) smem = 0;                  // never taken
+  if (smem < radix_smem<E>()) smem = radix_smem<E>();
+  if (smem < bucket_smem<E>()) smem = bucket_smem<E>();
+  return smem;
 }
 
-cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t rows,
-                               const int32_t* row_starts, const int32_t* row_lens, int32_t k,
-                               int32_t* idx, uint32_t* dev_status, cudaStream_t stream) {
+size_t topk_smem_bytes(int64_t row_stride, int k) {
+  return short_rows(row_stride) ? smem_bytes<6>(row_stride, k) : smem_bytes<8>(row_stride, k);
+}
+
+template <int E>
+static cudaError_t launch(const float* logits, int64_t row_stride, int32_t rows,
+                          const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                          int32_t* idx, uint32_t* dev_status, cudaStream_t stream) {
   const int64_t cap = row_stride < k ? row_stride : k;
   int sort_n = 2;
   while (sort_n < cap) sort_n <<= 1;
-  size_t smem = 8 * (size_t)sort_n + 4 * (size_t)row_stride;
-  if (smem < kRadixSmem) smem = kRadixSmem;
-  if (smem < kBucketSmem) smem = kBucketSmem;
+  const size_t smem = smem_bytes<E>(row_stride, k);
   // The shared-memory limit is a per-device attribute of the kernel; raise it only when
   // a call needs more than a previous call on this device set (races only repeat it).
   static std::atomic<int> configured[64];
@@ -556,26 +595,37 @@ cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_relaxed) < (int)smem) {
-    e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(topk_select_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store((int)smem, std::memory_order_relaxed);
   }
-  topk_select_kernel<<<rows, kTopkThreads, smem, stream>>>(logits, row_stride, row_starts,
-                                                            row_lens, k, sort_n, idx, dev_status);
+  topk_select_kernel<E><<<rows, kTopkThreads, smem, stream>>>(logits, row_stride, row_starts,
+                                                               row_lens, k, sort_n, idx,
+                                                               dev_status);
   e = cudaGetLastError();
   if (e == cudaErrorInvalidValue) {
     // A new context (after a device reset, say) starts from the default limit: set it
     // and launch once more (the refused launch ran nothing).
-    e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(topk_select_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    topk_select_kernel<<<rows, kTopkThreads, smem, stream>>>(logits, row_stride, row_starts,
-                                                              row_lens, k, sort_n, idx,
-                                                              dev_status);
+    topk_select_kernel<E><<<rows, kTopkThreads, smem, stream>>>(logits, row_stride, row_starts,
+                                                                 row_lens, k, sort_n, idx,
+                                                                 dev_status);
     e = cudaGetLastError();
   }
   return e;
+}
+
+cudaError_t launch_topk_select(const float* logits, int64_t row_stride, int32_t rows,
+                               const int32_t* row_starts, const int32_t* row_lens, int32_t k,
+                               int32_t* idx, uint32_t* dev_status, cudaStream_t stream) {
+  return short_rows(row_stride)
+             ? launch<6>(logits, row_stride, rows, row_starts, row_lens, k, idx, dev_status,
+                         stream)
+             : launch<8>(logits, row_stride, rows, row_starts, row_lens, k, idx, dev_status,
+                         stream);
 }
 
 }  // namespace tts
