@@ -143,3 +143,24 @@ def test_bucket_limit_and_mixed_values(tts):
                         torch.full((2,), 4096, dtype=torch.int32), 4000)
     ref, _ = oracle_idx(full)
     assert np.array_equal(run(tts, full).cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("cols", [3071, 3072, 3073])
+def test_per_thread_shape_boundary(tts, cols):
+    # Rows of at most 3072 values run with six values per thread (four CTAs per SM),
+    # longer ones with eight; either side of the boundary, whole and partial windows of
+    # bf16-grid values (buckets of ties), a row of two values only (the radix fallback)
+    # and a row that ends exactly at the last thread's last value.
+    g = torch.Generator().manual_seed(cols)
+    x = torch.randn(6, cols, generator=g).to(torch.bfloat16).float()
+    x[1] = torch.where(torch.rand(cols, generator=g) < 0.5, torch.tensor(1.0), torch.tensor(-2.5))
+    starts = torch.tensor([0, 0, 1, cols - 1, 0, 7], dtype=torch.int32)
+    lens = torch.tensor([cols, cols, cols - 1, 1, 2048, cols - 7], dtype=torch.int32)
+    for k in (1, 2048, 3072):
+        inp = W.TopkInputs(x, starts, lens, k)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        got = run(tts, inp, st).cpu().numpy()
+        ref, bad = oracle_idx(inp)
+        assert bad == 0
+        tts.check_status(st)
+        assert np.array_equal(got, ref), f"cols {cols} k {k}"

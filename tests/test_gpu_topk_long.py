@@ -89,3 +89,24 @@ def test_matches_the_one_cta_kernel(tts):
     dev = torch.device("cuda")
     a = tts.topk_select(inp.logits.to(dev), inp.row_starts.to(dev), inp.row_lens.to(dev), inp.k)
     assert torch.equal(a, run(tts, inp))
+
+
+def test_picks_clustered_along_the_row(tts):
+    # The threshold comes from a sample spread evenly over the window; rows whose large
+    # values sit together (in the first 8192 values, in the first 16384, in the later
+    # half) or rise steadily along the row make the sample's view of the row uneven:
+    # the selection must still be exact.
+    g = torch.Generator().manual_seed(23)
+    rows, cols = 4, 262144
+    x = torch.randn(rows, cols, generator=g).to(torch.bfloat16).float()
+    x[0, :8192] += 10.0                                  # every pick in the first round
+    x[1, :16384] += 10.0                                 # first chunk, beyond its first round
+    x[2, cols // 2:] += 5.0                              # the later half dominates
+    x[3] = torch.linspace(-3.0, 3.0, cols).to(torch.bfloat16).float() + 0.01 * x[3]
+    inp = W.TopkInputs(x, torch.zeros(rows, dtype=torch.int32),
+                       torch.full((rows,), cols, dtype=torch.int32), 2048)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run(tts, inp, st)
+    tts.check_status(st)
+    ref, _ = oracle_idx(inp)
+    assert np.array_equal(got.cpu().numpy(), ref)

@@ -10,24 +10,25 @@
 // Values map to order-preserving 32-bit keys (-0 folded onto +0); a key and its position
 // travel as the 64-bit composite key << 32 | ~position, which orders exactly as the
 // definition does (key descending, then position ascending) and is unique. Sample-select,
-// two launches in stream order (after a reset of the per-row counts):
-//   1. sample: every CTA of a row reads the same 32-value blocks spread evenly over the
-//      window (4096 values at most), histograms their keys' top 12 bits and takes as
-//      threshold t the lower bound of the bucket where the sample's count from the top
-//      reaches the share of 1.5 * min(k, len) + 256 values; windows of up to kCap values
-//      take t = 0. So all CTAs of a row agree on t without waiting for one another.
-//   2. compact: one CTA per (row, chunk) streams the window once and appends every
-//      composite with key >= t to the row's candidate array (gathered per CTA in shared
-//      memory, placed by one integer atomic per CTA: the order in the array is
+// two launches in stream order (after a reset of each row's header):
+//   1. compact: one CTA per (row, chunk). Every CTA of a row first reads the same
+//      32-value blocks spread evenly over the window (4096 values at most), histograms
+//      their keys' top 12 bits and takes as threshold t the lower bound of the bucket
+//      where the sample's count from the top reaches its share of 1.5 * min(k, len) +
+//      256 values (windows of up to kCap values take t = 0), so all CTAs of a row agree
+//      on t without waiting for one another. It then streams its chunk once and appends
+//      every value with key >= t to the row's candidate array (gathered per CTA in
+//      shared memory, placed by one integer atomic per CTA: the order in the array is
 //      arbitrary, its contents are not).
-//   3. finish: one CTA per row. If the candidates hold at least min(k, len) composites
-//      and fit the array, every selected composite is among them (at least min(k, len)
-//      keys are >= t, so the min(k, len)-th largest key is too): an MSB-first radix
-//      select over the 64-bit composites finds the min(k, len)-th largest, C; the
-//      composites >= C are sorted descending (bitonic network) and their positions
-//      written. Else (the sample misjudged the row, e.g. a row piling up on one value)
-//      the CTA finds the picks exactly on its own: a radix select over the window's
-//      keys, a collect that ranks ties by position, and the same sort.
+//   2. finish: one CTA per row. If the candidates number at least min(k, len) and fit
+//      the array, every selected composite is among them (at least min(k, len) keys are
+//      >= t, so the min(k, len)-th largest key is too). They are ranked by buckets: a
+//      counting pass over their keys, a scan, and each member of a bucket that starts
+//      before min(k, len) placed at its bucket's start plus the number of larger
+//      composites in its bucket (a row piling up on a few values takes an MSB-first
+//      radix select over the composites and a bitonic sort instead). Else (the sample
+//      misjudged the row) the CTA finds the picks exactly on its own: a radix select
+//      over the window's keys, a collect that ranks ties by position, and the sort.
 // Either way the result is fully determined by the input, and no CTA waits for another.
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -105,13 +106,15 @@ __device__ __forceinline__ int scan_excl(int v, int* warp_tot, int* total) {
 // The row's threshold key from its sample (block-collective; every CTA of a row computes
 // the same value from the same values): the lower bound of the 12-bit key bucket where
 // the sample's count from the top reaches its share of 1.5 * take + 256 values.
-__device__ uint32_t sample_threshold(const float* __restrict__ x, int64_t len, int64_t take,
+// Windows are at most 2^30 long, so 32-bit arithmetic holds every quantity here.
+__device__ uint32_t sample_threshold(const float* __restrict__ x, uint32_t len, uint32_t take,
                                      uint32_t* hist, int* warp_tot, uint32_t* s_t) {
-  int64_t nb = len / 32;
+  uint32_t nb = len / 32;
   if (nb > kSampleBlocks) nb = kSampleBlocks;
-  const int64_t stride = len / nb;  // >= 32
-  const int64_t ns = 32 * nb;
-  int64_t want = ((3 * take / 2 + 256) * ns + len - 1) / len;  // rounded up
+  const uint32_t stride = len / nb;  // >= 32
+  const uint32_t ns = 32 * nb;       // <= 4096
+  // ceil((1.5 take + 256) ns / len): the product is below 6400 * 4096 < 2^32.
+  uint32_t want = ((3 * take / 2 + 256) * ns + len - 1) / len;
   if (want > ns) want = ns;
   for (int b = threadIdx.x; b < (1 << kSampleBits); b += kLThreads) hist[b] = 0u;
   if (threadIdx.x == 0) *s_t = 0u;  // sample too small to reach `want`: every key
@@ -121,12 +124,12 @@ __device__ uint32_t sample_threshold(const float* __restrict__ x, int64_t len, i
   float sv[kPerThread];
 #pragma unroll
   for (int u = 0; u < kPerThread; ++u) {
-    const int64_t s = (int64_t)u * kLThreads + threadIdx.x;
-    sv[u] = (s < ns) ? __ldg(x + (s >> 5) * stride + (s & 31)) : 0.f;
+    const uint32_t s = u * kLThreads + threadIdx.x;  // (s >> 5) * stride + 31 < len
+    sv[u] = (s < ns) ? __ldg(x + ((s >> 5) * stride + (s & 31))) : 0.f;
   }
 #pragma unroll
   for (int u = 0; u < kPerThread; ++u) {
-    const int64_t s = (int64_t)u * kLThreads + threadIdx.x;
+    const uint32_t s = u * kLThreads + threadIdx.x;
     if (s < ns) atomicAdd(&hist[key_of(sv[u]) >> (32 - kSampleBits)], 1u);
   }
   __syncthreads();
@@ -143,7 +146,7 @@ __device__ uint32_t sample_threshold(const float* __restrict__ x, int64_t len, i
   int run = scan_excl<kLWarps>(sum, warp_tot, &tot);
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    if (run < want && want <= run + (int)c[q])
+    if (run < (int)want && (int)want <= run + (int)c[q])
       *s_t = (uint32_t)((1 << kSampleBits) - 1 - kPer * (int)threadIdx.x - q) << (32 - kSampleBits);
     run += (int)c[q];
   }
@@ -161,7 +164,7 @@ constexpr int kLocal = 3072;
 __global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
     const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
     const int32_t* __restrict__ row_lens, int k, int g, int64_t chunk_len, uint8_t* ws) {
-  __shared__ uint64_t local[kLocal];
+  __shared__ uint2 local[kLocal];  // candidates: (value bits, window position)
   __shared__ uint32_t hist[1 << kSampleBits];
   __shared__ int warp_tot[kLWarps];
   __shared__ uint32_t s_n, s_base, s_t;
@@ -176,23 +179,47 @@ __global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
   uint64_t* cand = row_cand(ws, row);
   const float* x = logits + row * row_stride + st;
   const int64_t take = len < k ? len : k;
-  const uint32_t t = len <= kCap ? 0u : sample_threshold(x, len, take, hist, warp_tot, &s_t);
+  const uint32_t t =
+      len <= kCap ? 0u : sample_threshold(x, (uint32_t)len, (uint32_t)take, hist, warp_tot, &s_t);
   if (threadIdx.x == 0) s_n = 0u;
   __syncthreads();
   // key(x) >= t  <=>  x >= the float whose key is t (keys order as the floats do, -0 and
-  // +0 alike), so each value costs one float comparison; only the candidates (a few per
-  // cent) compute their key and take a slot. t = 0 takes every value.
+  // +0 alike), so each value costs one float comparison. A warp whose lanes hold no
+  // candidate moves on after one ballot; otherwise each lane with candidates takes a
+  // slot per candidate (a few per cent of the values) and keeps its bits and position;
+  // keys and composites are formed once per candidate, on the copy out. t = 0 takes
+  // every value.
   const bool all = t == 0u;
   const float tf = __uint_as_float((t & 0x80000000u) ? (t & 0x7FFFFFFFu) : ~t);
-  auto consider = [&](bool valid, float v, int64_t j) {
-    if (valid && (all || v >= tf)) {
-      const uint32_t slot = atomicAdd(&s_n, 1u);
-      if (slot < (uint32_t)kLocal) local[slot] = comp_of(key_of(v), j);
+  auto put = [&](float v, int64_t j) {  // every value taken: slots follow the positions
+    const uint32_t slot = all ? (uint32_t)(j - c0) : atomicAdd(&s_n, 1u);
+    if (slot < (uint32_t)kLocal) local[slot] = make_uint2(__float_as_uint(v), (uint32_t)j);
+  };
+  auto take4 = [&](float4 v, int64_t j, int valid) {  // valid: how many of the 4 are in
+    const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    const bool any = valid > 0 && (all || m >= tf);
+    if (__ballot_sync(0xFFFFFFFFu, any) == 0u) return;  // warp-uniform
+    if (any) {
+      if (all || v.x >= tf) put(v.x, j);
+      if (valid > 1 && (all || v.y >= tf)) put(v.y, j + 1);
+      if (valid > 2 && (all || v.z >= tf)) put(v.z, j + 2);
+      if (valid > 3 && (all || v.w >= tf)) put(v.w, j + 3);
     }
   };
-  // Vector loads when the chunk starts on a 16-byte boundary (the whole CTA agrees).
+  // Whole rounds of loads without bounds checks, then a checked last round. Vector loads
+  // when the chunk starts on a 16-byte boundary (the whole CTA agrees).
   if ((reinterpret_cast<uintptr_t>(x + c0) & 15) == 0) {
-    for (int64_t j0 = c0; j0 < c1; j0 += 4 * kLThreads * kUnroll4) {
+    constexpr int64_t kStep = 4 * kLThreads * kUnroll4;
+    int64_t j0 = c0;
+    for (; j0 + kStep <= c1; j0 += kStep) {
+      const float4* x4 = reinterpret_cast<const float4*>(x + j0) + threadIdx.x;
+      float4 v[kUnroll4];
+#pragma unroll
+      for (int u = 0; u < kUnroll4; ++u) v[u] = __ldg(x4 + u * kLThreads);
+#pragma unroll
+      for (int u = 0; u < kUnroll4; ++u) take4(v[u], j0 + 4 * (u * kLThreads + threadIdx.x), 4);
+    }
+    for (; j0 < c1; j0 += kStep) {
       float4 v[kUnroll4];
 #pragma unroll
       for (int u = 0; u < kUnroll4; ++u) {
@@ -205,14 +232,26 @@ __global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
 #pragma unroll
       for (int u = 0; u < kUnroll4; ++u) {
         const int64_t j = j0 + 4 * (u * kLThreads + threadIdx.x);
-        consider(j < c1, v[u].x, j);
-        consider(j + 1 < c1, v[u].y, j + 1);
-        consider(j + 2 < c1, v[u].z, j + 2);
-        consider(j + 3 < c1, v[u].w, j + 3);
+        const int64_t in = c1 - j;
+        take4(v[u], j, in <= 0 ? 0 : (in >= 4 ? 4 : (int)in));
       }
     }
   } else {
-    for (int64_t j0 = c0; j0 < c1; j0 += kLThreads * kUnroll) {
+    constexpr int64_t kStep = kLThreads * kUnroll;
+    auto take1 = [&](float v, int64_t j, bool ok) {
+      const bool c = ok && (all || v >= tf);
+      if (__ballot_sync(0xFFFFFFFFu, c) == 0u) return;  // warp-uniform
+      if (c) put(v, j);
+    };
+    int64_t j0 = c0;
+    for (; j0 + kStep <= c1; j0 += kStep) {
+      float v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(x + j0 + u * kLThreads + threadIdx.x);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) take1(v[u], j0 + u * kLThreads + threadIdx.x, true);
+    }
+    for (; j0 < c1; j0 += kStep) {
       float v[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
@@ -222,10 +261,11 @@ __global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t j = j0 + u * kLThreads + threadIdx.x;
-        consider(j < c1, v[u], j);
+        take1(v[u], j, j < c1);
       }
     }
   }
+  if (all && threadIdx.x == 0) s_n = (uint32_t)(c1 - c0);
   __syncthreads();
   const uint32_t n = s_n;
   if (n == 0) return;
@@ -235,10 +275,33 @@ __global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
   if (n > (uint32_t)kLocal) return;
   const uint32_t base = s_base;
   for (uint32_t i = threadIdx.x; i < n; i += kLThreads)
-    if (base + i < (uint32_t)kCap) cand[base + i] = local[i];
+    if (base + i < (uint32_t)kCap) {
+      const uint2 c = local[i];
+      cand[base + i] = comp_of(key_of(__uint_as_float(c.x)), c.y);
+    }
 }
 
 // ---------------------------------------------------------------------------- 3. finish
+// Bucket-rank selection of the candidates (the way the one-CTA kernel ranks short
+// windows): the candidates' keys are mapped linearly onto kFBuckets buckets in
+// descending key order; a counting pass and a scan place every bucket, the buckets that
+// start before `take` are filled (atomic cursors: any order inside a bucket), and each
+// member's output place is its bucket's start plus the number of larger composites in
+// its bucket. Buckets hold a value's ties (the row's many copies of one bf16 value, ~20
+// among the picks of a normal row), so the comparisons stay few; a selectable bucket of
+// more than kFMaxBucket members sends the row to the radix select and bitonic sort.
+constexpr int kFBuckets = 4096;
+constexpr int kFBucketBits = 12;
+constexpr uint32_t kFMaxBucket = 512;
+constexpr int kFSlots = kMaxTake + kFMaxBucket;  // selectable members, at most
+static_assert(kFBuckets == 4 * kFinishThreads, "one uint4 of counters per thread");
+// Shared memory after the kCap candidates: per bucket its count / start | end, the
+// insertion cursors, then the placed members' composites and their buckets' words. The
+// radix path's picks (kMaxTake composites) reuse the same bytes.
+constexpr size_t kFRegion = 4 * kFBuckets * 2 + (8 + 4) * (size_t)kFSlots;
+static_assert(kFRegion >= 8 * (size_t)kMaxTake, "the picks fit the bucket region");
+constexpr size_t kFinishSmem = 8 * (size_t)kCap + kFRegion;
+
 // Bitonic sort, descending, of the n = E * kFinishThreads composites in buf (E = 2 or 4),
 // whose result it writes to out as positions (the first `take`, then -1 up to k). Thread
 // t holds elements t E .. t E + E - 1 in registers. Compare-exchanges between elements of
@@ -379,11 +442,13 @@ __global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
     const float* __restrict__ logits, int64_t row_stride, const int32_t* __restrict__ row_starts,
     const int32_t* __restrict__ row_lens, int k, uint8_t* ws, int32_t* __restrict__ idx,
     uint32_t* status) {
-  extern __shared__ __align__(16) uint64_t sel[];  // [kCap] candidates, [kMaxTake] picks
+  extern __shared__ __align__(16) uint64_t sel[];  // [kCap] candidates, then kFRegion bytes
   __shared__ int hist[256];
   __shared__ int warp_tot[kFWarps];
   __shared__ int s_digit, s_above, s_n;
   __shared__ unsigned long long s_or, s_and;
+  __shared__ uint32_t s_kmin, s_kmax, s_maxc, s_ranked;
+  __shared__ uint32_t s_wsum[kFWarps];
   const int64_t row = blockIdx.x;
   const int64_t st = row_starts[row], len = row_lens[row];
   int32_t* out = idx + row * (int64_t)k;
@@ -395,90 +460,175 @@ __global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
   const int take = (int)(len < k ? len : k);
   const int64_t cnt = (int64_t)__ldcg(row_head(ws, row) + 1);
   uint64_t* const picks = sel + kCap;  // [kMaxTake]: the selected composites, to sort
-  if (cnt >= take && cnt <= kCap) {
+  // The candidates decide the row unless they are too few (the sample misjudged the
+  // row) or too many for the array.
+  const bool exact = !(cnt >= take && cnt <= kCap);
+  if (!exact) {
     const int n = (int)cnt;
     const uint64_t* cand = row_cand(ws, row);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t* const se = reinterpret_cast<uint32_t*>(sel + kCap);        // [kFBuckets]
+    uint32_t* const cur = se + kFBuckets;                                 // [kFBuckets]
+    uint64_t* const slot_c = reinterpret_cast<uint64_t*>(cur + kFBuckets);  // [kFSlots]
+    uint32_t* const slot_w = reinterpret_cast<uint32_t*>(slot_c + kFSlots);  // [kFSlots]
     // Load, with a census of the bits (OR / AND) so that bytes on which every candidate
-    // agrees need no pass below.
+    // agrees need no radix pass, and the keys' range for the buckets.
+    reinterpret_cast<uint4*>(se)[tid] = make_uint4(0u, 0u, 0u, 0u);
     unsigned long long c_or = 0ull, c_and = ~0ull;
-    for (int j = threadIdx.x; j < n; j += kFinishThreads) {
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    for (int j = tid; j < n; j += kFinishThreads) {
       const uint64_t c = __ldcg(cand + j);
       sel[j] = c;
       c_or |= c;
       c_and &= c;
+      kmin = min(kmin, static_cast<uint32_t>(c >> 32));
+      kmax = max(kmax, static_cast<uint32_t>(c >> 32));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       c_or |= __shfl_xor_sync(0xFFFFFFFFu, c_or, o);
       c_and &= __shfl_xor_sync(0xFFFFFFFFu, c_and, o);
     }
-    if (threadIdx.x == 0) {
+    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    if (tid == 0) {
       s_or = 0ull;
       s_and = ~0ull;
+      s_kmin = 0xFFFFFFFFu;
+      s_kmax = 0u;
+      s_maxc = 0u;
+      s_ranked = static_cast<uint32_t>(n);
     }
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) {
+    if (lane == 0) {
       atomicOr(&s_or, c_or);
       atomicAnd(&s_and, c_and);
+      atomicMin(&s_kmin, kmin);
+      atomicMax(&s_kmax, kmax);
     }
     __syncthreads();
-    const uint64_t varying = s_or ^ s_and, common = s_and;
-    // The take-th largest composite C among the candidates (they are unique): an
-    // MSB-first radix select over the 64 bits, then every composite >= C is a pick.
-    uint64_t prefix = 0, mask = 0;
-    int remaining = take;
-    for (int pass = 0; pass < 8 && n > take; ++pass) {
-      const int shift = 56 - 8 * pass;
-      if (((varying >> shift) & 0xFFu) == 0) {  // the same byte in every candidate
-        prefix |= common & (0xFFull << shift);
-        mask |= 0xFFull << shift;
-        continue;
+    // Bucket of key y: (kmax - y) >> sh, so bucket order is descending key order.
+    const uint32_t bmax = s_kmax, span = bmax - s_kmin;
+    const int sh = max(0, (32 - __clz(span)) - kFBucketBits);
+    for (int j = tid; j < n; j += kFinishThreads)
+      atomicAdd(&se[(bmax - static_cast<uint32_t>(sel[j] >> 32)) >> sh], 1u);
+    __syncthreads();
+    {  // exclusive scan: thread tid owns buckets 4 tid .. 4 tid + 3; counts < 2^16
+      const uint4 c4 = reinterpret_cast<const uint4*>(se)[tid];
+      const uint32_t w[4] = {c4.x, c4.y, c4.z, c4.w};
+      const uint32_t tot = w[0] + w[1] + w[2] + w[3];
+      uint32_t x = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
       }
-      for (int b = threadIdx.x; b < 256; b += kFinishThreads) hist[b] = 0;
+      if (lane == 31) s_wsum[warp] = x;
+      __syncthreads();
+      uint32_t run = x - tot + __reduce_add_sync(0xFFFFFFFFu, lane < warp ? s_wsum[lane] : 0u);
+      const uint32_t tk = static_cast<uint32_t>(take);
+      uint32_t o[4], mx = 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t e = run + w[q];
+        o[q] = run | (e << 16);
+        if (run < tk) mx = max(mx, w[q]);  // only buckets that start before take count
+        if (run < tk && tk <= e) s_ranked = e;
+        run = e;
+      }
+      mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+      if (lane == 0) atomicMax(&s_maxc, mx);
+      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+      reinterpret_cast<uint4*>(se)[tid] = ov;
+      reinterpret_cast<uint4*>(cur)[tid] = ov;
+    }
+    __syncthreads();
+    if (s_maxc <= kFMaxBucket) {  // uniform
+      const uint32_t ranked = s_ranked;  // <= take + kFMaxBucket
+      for (int j = tid; j < n; j += kFinishThreads) {
+        const uint64_t c = sel[j];
+        const uint32_t b = (bmax - static_cast<uint32_t>(c >> 32)) >> sh;
+        const uint32_t bw = se[b];
+        if ((bw & 0xFFFFu) < static_cast<uint32_t>(take)) {
+          const uint32_t slot = atomicAdd(&cur[b], 1u) & 0xFFFFu;
+          slot_c[slot] = c;
+          slot_w[slot] = bw;
+        }
+      }
+      __syncthreads();
+      // Rank in bucket order: thread t takes slots t, t + kFinishThreads, ...
+      for (uint32_t j = tid; j < ranked; j += kFinishThreads) {
+        const uint64_t me = slot_c[j];
+        const uint32_t bw = slot_w[j], s0 = bw & 0xFFFFu;
+        uint32_t rank = 0;
+        const uint64_t* const end = slot_c + (bw >> 16);
+#pragma unroll 1
+        for (const uint64_t* m = slot_c + s0; m < end; ++m) rank += *m > me ? 1u : 0u;
+        const uint32_t dst = s0 + rank;
+        if (dst < static_cast<uint32_t>(take))
+          out[dst] = static_cast<int32_t>(~static_cast<uint32_t>(me & 0xFFFFFFFFull));
+      }
+      for (int e = take + tid; e < k; e += kFinishThreads) out[e] = -1;
+      return;
+    } else {
+      const uint64_t varying = s_or ^ s_and, common = s_and;
+      // The take-th largest composite C among the candidates (they are unique): an
+      // MSB-first radix select over the 64 bits, then every composite >= C is a pick.
+      uint64_t prefix = 0, mask = 0;
+      int remaining = take;
+      for (int pass = 0; pass < 8 && n > take; ++pass) {
+        const int shift = 56 - 8 * pass;
+        if (((varying >> shift) & 0xFFu) == 0) {  // the same byte in every candidate
+          prefix |= common & (0xFFull << shift);
+          mask |= 0xFFull << shift;
+          continue;
+        }
+        for (int b = threadIdx.x; b < 256; b += kFinishThreads) hist[b] = 0;
+        __syncthreads();
+        for (int j = threadIdx.x; j < n; j += kFinishThreads) {
+          const uint64_t c = sel[j];
+          if ((c & mask) == prefix) atomicAdd(&hist[(int)((c >> shift) & 0xFFu)], 1);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {  // lane l owns bins 255 - 8l .. 248 - 8l (descending)
+          const int l = threadIdx.x;
+          int c[8], sum = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            c[q] = hist[255 - 8 * l - q];
+            sum += c[q];
+          }
+          int incl = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (l >= o) incl += y;
+          }
+          int above = incl - sum;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (above < remaining && remaining <= above + c[q]) {
+              s_digit = 255 - 8 * l - q;
+              s_above = above;
+            }
+            above += c[q];
+          }
+        }
+        __syncthreads();
+        remaining -= s_above;
+        prefix |= static_cast<uint64_t>(s_digit) << shift;
+        mask |= 0xFFull << shift;
+        __syncthreads();
+      }
+      const uint64_t C = (n > take) ? prefix : 0ull;  // n == take: every candidate
+      if (threadIdx.x == 0) s_n = 0;
       __syncthreads();
       for (int j = threadIdx.x; j < n; j += kFinishThreads) {
         const uint64_t c = sel[j];
-        if ((c & mask) == prefix) atomicAdd(&hist[(int)((c >> shift) & 0xFFu)], 1);
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) {  // lane l owns bins 255 - 8l .. 248 - 8l (descending)
-        const int l = threadIdx.x;
-        int c[8], sum = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          c[q] = hist[255 - 8 * l - q];
-          sum += c[q];
+        if (c >= C) {
+          const int slot = atomicAdd(&s_n, 1);
+          if (slot < take) picks[slot] = c;
         }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (l >= o) incl += y;
-        }
-        int above = incl - sum;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (above < remaining && remaining <= above + c[q]) {
-            s_digit = 255 - 8 * l - q;
-            s_above = above;
-          }
-          above += c[q];
-        }
-      }
-      __syncthreads();
-      remaining -= s_above;
-      prefix |= static_cast<uint64_t>(s_digit) << shift;
-      mask |= 0xFFull << shift;
-      __syncthreads();
-    }
-    const uint64_t C = (n > take) ? prefix : 0ull;  // n == take: every candidate
-    if (threadIdx.x == 0) s_n = 0;
-    __syncthreads();
-    for (int j = threadIdx.x; j < n; j += kFinishThreads) {
-      const uint64_t c = sel[j];
-      if (c >= C) {
-        const int slot = atomicAdd(&s_n, 1);
-        if (slot < take) picks[slot] = c;
       }
     }
   } else {  // the sample misjudged this row: select exactly from the window itself
@@ -533,7 +683,7 @@ cudaError_t launch_topk_long(const float* logits, int64_t row_stride, int32_t ro
       logits, row_stride, row_starts, row_lens, k, g, chunk_len, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = (size_t)(kCap + kMaxTake) * sizeof(uint64_t);
+  const size_t smem = kFinishSmem;
   e = cudaFuncSetAttribute(topk_long_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e != cudaSuccess) return e;
