@@ -141,8 +141,9 @@ tts_status tts_topk_select(const float* logits, int64_t row_stride, int32_t rows
  * (section 2.2). Sample-select in three launches: per row, a threshold key from a
  * sample of the window (1/32 of it at most); one pass over the window, split over
  * many CTAs, that keeps every value at or above the threshold (integer atomics
- * only); per row, a selection of the k largest kept values by (value, position)
- * and a sort of them. A row the sample misjudges (fewer than min(k, len) kept,
+ * only); per row, the k largest kept values placed in (value, position) order by
+ * value buckets ranked inside (a radix select and a sort for rows piling up on a
+ * few values). A row the sample misjudges (fewer than min(k, len) kept,
  * or more than 16384, e.g. a row piling up on one value) is instead finished
  * exactly by one CTA straight from the window (radix select, ties ranked by
  * position): correct for every input, but a few passes over the row at one SM's
