@@ -507,11 +507,23 @@ __global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
       atomicMax(&s_kmax, kmax);
     }
     __syncthreads();
-    // Bucket of key y: (kmax - y) >> sh, so bucket order is descending key order.
+    // Bucket order is (key descending, position ascending) order. Keys are mapped
+    // linearly: bucket (kmax - key) >> sh. When the keys take fewer than 256 distinct
+    // values (all candidates share the key's low tz bits, and the span holds fewer than
+    // 256 steps of 2^tz), every key gets 16 buckets of its own, one per sixteenth of the
+    // window in position order, which splits the ties of one value (the many copies of a
+    // bf16 value among a normal row's picks) into groups ranked separately.
     const uint32_t bmax = s_kmax, span = bmax - s_kmin;
-    const int sh = max(0, (32 - __clz(span)) - kFBucketBits);
-    for (int j = tid; j < n; j += kFinishThreads)
-      atomicAdd(&se[(bmax - static_cast<uint32_t>(sel[j] >> 32)) >> sh], 1u);
+    const uint32_t kvary = static_cast<uint32_t>((s_or ^ s_and) >> 32);
+    const int tz = kvary != 0u ? __ffs(kvary) - 1 : 0;
+    const bool split = (span >> tz) < (uint32_t)(kFBuckets / 16);  // uniform
+    const int sh = split ? tz : max(0, (32 - __clz(span)) - kFBucketBits);
+    const int psh = max(0, (32 - __clz(static_cast<uint32_t>(len - 1))) - 4);
+    auto bucket_of = [&](uint64_t c) -> uint32_t {
+      const uint32_t kb = (bmax - static_cast<uint32_t>(c >> 32)) >> sh;
+      return split ? (kb << 4) | ((~static_cast<uint32_t>(c)) >> psh) : kb;
+    };
+    for (int j = tid; j < n; j += kFinishThreads) atomicAdd(&se[bucket_of(sel[j])], 1u);
     __syncthreads();
     {  // exclusive scan: thread tid owns buckets 4 tid .. 4 tid + 3; counts < 2^16
       const uint4 c4 = reinterpret_cast<const uint4*>(se)[tid];
@@ -547,7 +559,7 @@ __global__ void __launch_bounds__(kFinishThreads) topk_long_finish_kernel(
       const uint32_t ranked = s_ranked;  // <= take + kFMaxBucket
       for (int j = tid; j < n; j += kFinishThreads) {
         const uint64_t c = sel[j];
-        const uint32_t b = (bmax - static_cast<uint32_t>(c >> 32)) >> sh;
+        const uint32_t b = bucket_of(c);
         const uint32_t bw = se[b];
         if ((bw & 0xFFFFu) < static_cast<uint32_t>(take)) {
           const uint32_t slot = atomicAdd(&cur[b], 1u) & 0xFFFFu;
