@@ -110,3 +110,20 @@ def test_picks_clustered_along_the_row(tts):
     tts.check_status(st)
     ref, _ = oracle_idx(inp)
     assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_finish_radix_fallback_for_crowded_buckets(tts):
+    # 600 copies of one large value among the picks: a bucket of more than 512 members
+    # sends the finish to its radix select and sort. Row 0 lies on the bf16 grid (the
+    # finish splits a value's ties by position: the copies sit in one sixteenth of the
+    # row); row 1 holds plain fp32 values (no split: the copies are spread over the row).
+    g = torch.Generator().manual_seed(29)
+    cols = 262144
+    x = torch.randn(2, cols, generator=g)
+    x[0] = x[0].to(torch.bfloat16).float()
+    x[0, 100:700] = 4.0
+    x[1, torch.randperm(cols, generator=g)[:600]] = 4.0
+    inp = W.TopkInputs(x, torch.zeros(2, dtype=torch.int32),
+                       torch.full((2,), cols, dtype=torch.int32), 2048)
+    ref, _ = oracle_idx(inp)
+    assert np.array_equal(run(tts, inp).cpu().numpy(), ref)
