@@ -253,11 +253,11 @@ __device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* 
   static_assert(sort_max<E>() <= 4096, "positions must fit the composite's 12 bits");
   uint32_t* const se = reinterpret_cast<uint32_t*>(smem);              // [kBuckets]
   uint2* const slots = reinterpret_cast<uint2*>(smem + 4 * kBuckets);  // [kSortMax]
-  __shared__ uint32_t s_rng[4];  // min / max skey of the non-negative half, then the negative
+  // Per warp: min / max skey of the non-negative half, then of the negative half.
+  __shared__ uint4 s_wrng[kWarps];
   __shared__ uint32_t s_maxc, s_ranked;
   __shared__ uint32_t s_wsum[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 4) s_rng[tid] = (tid & 1) ? 0u : 0xFFFFFFFFu;
   if (tid == 0) {
     s_maxc = 0u;
     s_ranked = static_cast<uint32_t>(n);
@@ -292,19 +292,20 @@ __device__ __forceinline__ bool bucket_topk(Value value, int n, int k, int32_t* 
   pmax = __reduce_max_sync(0xFFFFFFFFu, pmax);
   nmin = __reduce_min_sync(0xFFFFFFFFu, nmin);
   nmax = __reduce_max_sync(0xFFFFFFFFu, nmax);
-  __syncthreads();
-  if (lane == 0) {
-    atomicMin(&s_rng[0], pmin);
-    atomicMax(&s_rng[1], pmax);
-    atomicMin(&s_rng[2], nmin);
-    atomicMax(&s_rng[3], nmax);
+  if (lane == 0) s_wrng[warp] = make_uint4(pmin, pmax, nmin, nmax);
+  __syncthreads();  // also: the bucket counters are zeroed
+  {  // every warp reduces the warps' ranges itself (lane w reads warp w's)
+    const uint4 r = lane < kWarps ? s_wrng[lane] : make_uint4(0xFFFFFFFFu, 0u, 0xFFFFFFFFu, 0u);
+    pmin = __reduce_min_sync(0xFFFFFFFFu, r.x);
+    pmax = __reduce_max_sync(0xFFFFFFFFu, r.y);
+    nmin = __reduce_min_sync(0xFFFFFFFFu, r.z);
+    nmax = __reduce_max_sync(0xFFFFFFFFu, r.w);
   }
-  __syncthreads();
   // Per half: its smallest key and the shift that maps its span onto kHalfBuckets buckets.
   // A half's span is below 2^31, so the shift is at most 20 and the composite (offset
   // inside the bucket << 12 | position) fits 32 bits.
-  const uint32_t base0 = s_rng[0], base1 = s_rng[2];
-  const uint32_t span0 = s_rng[1] - base0, span1 = s_rng[3] - base1;  // garbage if empty
+  const uint32_t base0 = pmin, base1 = nmin;
+  const uint32_t span0 = pmax - base0, span1 = nmax - base1;  // garbage if empty
   const int sh0 = max(0, (32 - __clz(span0)) - kHalfBits);
   const int sh1 = max(0, (32 - __clz(span1)) - kHalfBits);
   const uint32_t low0 = (1u << sh0) - 1u, low1 = (1u << sh1) - 1u;
