@@ -443,23 +443,25 @@ def topk_long_protocol(step, dev, peaks):
             "protocol": f"CUDA graph of {n_call} calls over 4 rotating input sets"}
 
 
-def decode_protocol(step, dev, peaks):
-    """Decode-shaped sparse attention outside the step: 64 requests, each with a
-    32768-token context (the paged cache's max_seq_len on p3) in its own shuffled pages of
-    64, one query, 2048 indices; then each request's next KV row is written through its
-    page table. The 2.4 GB KV pool and the queries come from a seeded device generator
+def decode_protocol(step, dev, peaks, nreq=64):
+    """Decode-shaped sparse attention outside the step: `nreq` requests (64; a small
+    batch of 8 shows the key split filling the SMs), each with a 32768-token context (the
+    paged cache's max_seq_len on p3) in its own shuffled pages of 64, one query, 2048
+    indices; then each request's next KV row is written through its page table. The KV
+    pool (2.4 GB for 64 requests) and the queries come from a seeded device generator
     (values do not affect the timing); page tables and index lists as in
-    workloads.sparse_decode_inputs. Two index sets alternate (302 MB of gathered rows,
-    > L2); 20 calls timed with CUDA events."""
+    workloads.sparse_decode_inputs. Index sets rotate so that a round of them gathers
+    about 300 MB (> L2); 20 calls timed with CUDA events."""
     t = step.tts
-    nreq, ctx, ps, topk, dqk, dv = 64, 32768, 64, 2048, 576, 512
+    ctx, ps, topk, dqk, dv = 32768, 64, 2048, 576, 512
     g = torch.Generator(device="cpu").manual_seed(W.SEEDS["decode"])
     per = ctx // ps + 1
     pool = nreq * per
     tables = torch.randperm(pool, generator=g).to(torch.int32).view(nreq, per).to(dev)
     lens = torch.full((nreq,), ctx, dtype=torch.int32, device=dev)
+    n_sets = max(2, -(-(300 << 20) // (nreq * topk * dqk * 2)))
     idx_sets = [torch.stack([torch.randperm(ctx, generator=g)[:topk] for _ in range(nreq)])
-                .to(torch.int32).to(dev) for _ in range(2)]
+                .to(torch.int32).to(dev) for _ in range(n_sets)]
     gd = torch.Generator(device=dev).manual_seed(W.SEEDS["decode"])
     kv = torch.randn(pool, ps, dqk, generator=gd, device=dev).to(torch.bfloat16)
     q = torch.randn(nreq, 128, dqk, generator=gd, device=dev).to(torch.bfloat16)
@@ -468,8 +470,9 @@ def decode_protocol(step, dev, peaks):
     lse = torch.empty((nreq, 128), dtype=torch.float32, device=dev)
     ws = torch.empty(max(t.sparse_workspace_bytes(nreq), 16), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(dqk)
-    call = lambda i: t.sparse_attn_decode(q, kv, tables, lens, idx_sets[i % 2], scale, dv=dv,
-                                          out=out, lse=lse, workspace=ws, status=step.status)
+    call = lambda i: t.sparse_attn_decode(q, kv, tables, lens, idx_sets[i % n_sets], scale,
+                                          dv=dv, out=out, lse=lse, workspace=ws,
+                                          status=step.status)
     s = torch.cuda.Stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -498,7 +501,8 @@ def decode_protocol(step, dev, peaks):
                         f"128 heads, {topk} indices", "us_per_call": us,
             "gathered_bytes": gathered, "gathered_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
             "tflops": flops / (us * 1e-6) / 1e12, "kv_write_us": us_w,
-            "protocol": "CUDA graph of 20 calls, two alternating index sets (302 MB gathered)"}
+            "protocol": f"CUDA graph of 20 calls over {n_sets} rotating index sets "
+                        f"({n_sets * gathered / 1e6:.0f} MB gathered per round)"}
 
 
 def qkv_rope_protocol(step, dev, peaks, flush):
@@ -869,6 +873,7 @@ def run_gpu(args, rank, world, local):
         tts.check_status(step.status, "bench qkv_rope protocol")
     if "sparse" in parts and rank == 0 and extra:
         comp["sparse_decode"] = decode_protocol(step, dev, peaks)
+        comp["sparse_decode_small"] = decode_protocol(step, dev, peaks, nreq=8)
         tts.check_status(step.status, "bench decode protocol")
         tts.check_status(step.status, "bench top-k protocol")
     dom = max(parts, key=lambda p: comp[p]["ms"])
