@@ -191,12 +191,13 @@ tts_status tts_topk_select_long(const float* logits, int64_t row_stride, int32_t
  *            query's canonical list (validated, sorted, resolved to physical rows) into
  *            the workspace, so the attention CTAs start gathering at once instead of
  *            sorting first (same lists, same results bit for bit); (2) the (query,
- *            V half) units of the last, partial wave of CTAs each run as 2 or 4 CTAs
- *            over consecutive tiles of the sorted list, and the last of them to finish
- *            merges their unnormalised results (the online-softmax merge, in part
- *            order). The result stays deterministic and order-invariant; split units
- *            round differently from unsplit ones. Owned by the caller; calls that may
- *            overlap on the GPU need separate workspaces.
+ *            V half) units of the last, partial wave of CTAs each run as 2 to 16 CTAs
+ *            (as many as fit that wave) over consecutive tiles of the sorted list, and
+ *            their unnormalised results are merged in part order (the online-softmax
+ *            merge) by the last of them to finish, or, beyond 4 parts, by a merge
+ *            launch of one CTA per (unit, 16 heads). The result stays deterministic and
+ *            order-invariant; split units round differently from unsplit ones. Owned by
+ *            the caller; calls that may overlap on the GPU need separate workspaces.
  * Built shape: num_heads = 128, dqk = 576, dv = 512, 1 <= topk <= 2048,
  * page_size >= 1 (TTS_ERR_UNSUPPORTED otherwise). q, kv_cache, out and workspace
  * 16-byte aligned.
@@ -217,7 +218,7 @@ tts_status tts_sparse_attn_paged(const void* q, int32_t nq, int32_t num_heads, i
  * the per-request page tables of the paged cache in "从 SGLang Kernel源码到 GPU
  * Trace" (section 2.2, PagedKVCache) under the sparse attention and index rule of
  * "推理引擎的蝴蝶效应" (sections 实验方法和结果, 进一步探索). With few requests, the
- * workspace lets every (request, V half) unit run as 2 or 4 CTAs over consecutive
+ * workspace lets every (request, V half) unit run as up to 16 CTAs over consecutive
  * tiles of its sorted list, merged in part order (split-KV with a fixed-order combine).
  *
  * q           device bf16 [nreq, num_heads, dqk]

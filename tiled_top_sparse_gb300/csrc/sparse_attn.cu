@@ -26,8 +26,9 @@
 // Both CTAs of a query compute all of S (each over the 9 slabs in its own fixed
 // order, so their roundings may differ) and accumulate O for their 256 V columns:
 // the S work is done twice so that no partial scores move between SMs. The (query,
-// half) units of the last, partial wave of CTAs can run as 2-4 parts over
-// consecutive tiles of the sorted list, merged in part order by the last to finish.
+// half) units of the last, partial wave of CTAs can run as 2-16 parts over
+// consecutive tiles of the sorted list, merged in part order (by the last part to
+// finish, or for more than four parts by a merge launch).
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -53,7 +54,12 @@ constexpr int kMaxTopk = 2048;
 constexpr int kMaxTiles = kMaxTopk / kTileN;         // 32
 constexpr int kCountCap = 16384;  // kv_len up to this uses a counting sort
 constexpr int kScratchInts = 2 * kKStage / 4;  // sort scratch: the K stages (80 KB)
-constexpr int kMaxParts = 4;
+constexpr int kMaxParts = 16;
+// Units split into at most this many parts are merged by their last part to finish;
+// wider splits (small batches) leave the merge to a launch of its own, spread over many
+// CTAs, since one CTA reading every part's partial O would take longer than the split
+// saves.
+constexpr int kKernelMergeParts = 4;
 // One partial result: O [128 heads][256 columns], then m [128] and l [128].
 constexpr int kSlotFloats = kHeads * 256 + 2 * kHeads;
 static_assert(kMaxTopk <= 4 * kThreads, "one round of four index loads per thread");
@@ -94,6 +100,59 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
+}
+
+// The merge of a split unit's parts (unnormalised O, m, l of each part, in the slots of
+// `slot0`), in part order:
+//   out = sum_p w_p O_p / sum_p w_p l_p,  w_p = 2^((m_p - M) * scale * log2 e),
+//   M = max_p m_p  (the online-softmax merge, with a fixed order).
+// merge_weights: head h's weights w_p / L into s_w[p * ld + hw] (and its lse, written by
+// the unit of the first V half).
+template <int P>
+__device__ __forceinline__ void merge_weights(const SparseParams& p, const float* slot0,
+                                              int nparts, int h, int n, int r, float* s_w,
+                                              int ld, int hw = -1) {
+  if (hw < 0) hw = h;
+  float mp[P], w[P];
+  float M = -INFINITY;
+#pragma unroll
+  for (int pp = 0; pp < P; ++pp)
+    if (pp < nparts) {
+      mp[pp] = __ldcg(slot0 + pp * kSlotFloats + kHeads * 256 + h);
+      M = fmaxf(M, mp[pp]);
+    }
+  float L = 0.f;
+#pragma unroll
+  for (int pp = 0; pp < P; ++pp)
+    if (pp < nparts) {
+      w[pp] = (mp[pp] == -INFINITY) ? 0.f : ex2_approx((mp[pp] - M) * p.scale_log2);
+      L += __ldcg(slot0 + pp * kSlotFloats + kHeads * 256 + kHeads + h) * w[pp];
+    }
+  const float inv_L = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+  for (int pp = 0; pp < P; ++pp)
+    if (pp < nparts) s_w[pp * ld + hw] = w[pp] * inv_L;
+  if (r == 0 && p.lse != nullptr)
+    p.lse[(int64_t)n * kHeads + h] =
+        (L > 0.f) ? M * p.scale + log2f(L) * 0.69314718055994531f : -INFINITY;
+}
+// merge_row_chunk: columns 4 c4 .. 4 c4 + 3 of head h's 256 (weights at row hw of s_w).
+template <int P>
+__device__ __forceinline__ void merge_row_chunk(const float* slot0, int nparts, const float* s_w,
+                                                int ld, int h, int hw, int c4, float* obase) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int pp = 0; pp < P; ++pp)
+    if (pp < nparts) {
+      const float4 v =
+          __ldcg(reinterpret_cast<const float4*>(slot0 + pp * kSlotFloats + h * 256) + c4);
+      const float wq = s_w[pp * ld + hw];
+      acc.x = fmaf(v.x, wq, acc.x);
+      acc.y = fmaf(v.y, wq, acc.y);
+      acc.z = fmaf(v.z, wq, acc.z);
+      acc.w = fmaf(v.w, wq, acc.w);
+    }
+  *reinterpret_cast<float4*>(obase + (int64_t)h * kDv + 4 * c4) = acc;
 }
 
 __device__ __forceinline__ int kslab_of(int r, int i) {  // i-th K-only slab (global id)
@@ -622,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (nparts == 1 && lane == 0) bulk_wait_read_all();  // the slices stay until read
   }
-  if (nparts > 1 && fine) {
+  if (nparts > 1 && nparts <= kKernelMergeParts && fine) {
     // The last part of the unit to finish merges all parts in part order:
     //   out = sum_p w_p O_p / sum_p w_p l_p,  w_p = 2^((m_p - M) * scale * log2 e),
     //   M = max_p m_p  (the online-softmax merge, with a fixed order).
@@ -635,48 +694,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* slot0 = p.partial + (int64_t)(u - p.n_main) * nparts * kSlotFloats;
       // merge weights [part][head], in the idle gather stages (the staging is done)
       float* s_w = reinterpret_cast<float*>(smem + kQhiBytes);
-      if (tid < kHeads) {
-        float mp[kMaxParts], w[kMaxParts];
-        float M = -INFINITY;
-#pragma unroll
-        for (int pp = 0; pp < kMaxParts; ++pp)
-          if (pp < nparts) {
-            mp[pp] = __ldcg(slot0 + pp * kSlotFloats + kHeads * 256 + tid);
-            M = fmaxf(M, mp[pp]);
-          }
-        float L = 0.f;
-#pragma unroll
-        for (int pp = 0; pp < kMaxParts; ++pp)
-          if (pp < nparts) {
-            w[pp] = (mp[pp] == -INFINITY) ? 0.f : ex2_approx((mp[pp] - M) * p.scale_log2);
-            L += __ldcg(slot0 + pp * kSlotFloats + kHeads * 256 + kHeads + tid) * w[pp];
-          }
-        const float inv_L = (L > 0.f) ? 1.f / L : 0.f;
-#pragma unroll
-        for (int pp = 0; pp < kMaxParts; ++pp)
-          if (pp < nparts) s_w[pp * kHeads + tid] = w[pp] * inv_L;
-        if (r == 0 && p.lse != nullptr)
-          p.lse[(int64_t)n * kHeads + tid] =
-              (L > 0.f) ? M * p.scale + log2f(L) * 0.69314718055994531f : -INFINITY;
-      }
+      if (tid < kHeads)
+        merge_weights<kKernelMergeParts>(p, slot0, nparts, tid, n, r, s_w, kHeads);
       __syncthreads();
       float* obase = p.out + (int64_t)n * kHeads * kDv + 256 * r;
-      for (int i = tid; i < kHeads * 64; i += kThreads) {
-        const int hh = i >> 6, c4 = i & 63;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int pp = 0; pp < kMaxParts; ++pp)
-          if (pp < nparts) {
-            const float4 v =
-                __ldcg(reinterpret_cast<const float4*>(slot0 + pp * kSlotFloats + hh * 256) + c4);
-            const float wq = s_w[pp * kHeads + hh];
-            acc.x = fmaf(v.x, wq, acc.x);
-            acc.y = fmaf(v.y, wq, acc.y);
-            acc.z = fmaf(v.z, wq, acc.z);
-            acc.w = fmaf(v.w, wq, acc.w);
-          }
-        *reinterpret_cast<float4*>(obase + (int64_t)hh * kDv + 4 * c4) = acc;
-      }
+      for (int i = tid; i < kHeads * 64; i += kThreads)
+        merge_row_chunk<kKernelMergeParts>(slot0, nparts, s_w, kHeads, i >> 6, i >> 6,
+                                           i & 63, obase);
     }
   }
   tc_fence_before();
@@ -685,6 +709,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// The merge of units split into more than kKernelMergeParts parts: one CTA per (split
+// unit, 16 heads), after the attention launch, with the in-kernel merge's arithmetic.
+constexpr int kMergeHeads = 16;
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads) sparse_merge_kernel(const SparseParams p) {
+  __shared__ float s_w[kMaxParts * kMergeHeads];
+  const int k = blockIdx.x / (kHeads / kMergeHeads);
+  const int h0 = (blockIdx.x % (kHeads / kMergeHeads)) * kMergeHeads;
+  const int u = p.n_main + k, n = u >> 1, r = u & 1;
+  const float* slot0 = p.partial + (int64_t)k * p.parts * kSlotFloats;
+  if (threadIdx.x < kMergeHeads)
+    merge_weights<kMaxParts>(p, slot0, p.parts, h0 + threadIdx.x, n, r, s_w, kMergeHeads,
+                             threadIdx.x);
+  __syncthreads();
+  float* obase = p.out + (int64_t)n * kHeads * kDv + 256 * r;
+  for (int i = threadIdx.x; i < kMergeHeads * 64; i += kMergeThreads)
+    merge_row_chunk<kMaxParts>(slot0, p.parts, s_w, kMergeHeads, h0 + (i >> 6), i >> 6, i & 63,
+                               obase);
 }
 
 // The canonical lists of every query ahead of the attention launch, one CTA per query,
@@ -705,7 +749,8 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // The split of the last wave: with U = 2 nq units on `sms` SMs, the U mod sms units of
-// the partial wave run as `parts` CTAs each (4 if they still fit in one wave, else 2).
+// the partial wave run as `parts` CTAs each, as many as still fit in one wave (at most
+// kMaxParts); a small batch (decode with few requests) so fills the SMs.
 struct SplitPlan {
   int tail = 0, parts = 1;
   size_t done_bytes = 0, bytes = 0;
@@ -715,14 +760,13 @@ SplitPlan plan_split(int nq, int sms) {
   const int units = 2 * nq;
   const int tail = sms > 0 ? units % sms : 0;
   if (tail == 0) return s;
-  for (int parts = kMaxParts; parts >= 2; parts /= 2)
-    if (tail * parts <= sms) {
-      s.tail = tail;
-      s.parts = parts;
-      s.done_bytes = ((size_t)tail * 4 + 255) / 256 * 256;
-      s.bytes = s.done_bytes + (size_t)tail * parts * kSlotFloats * sizeof(float);
-      break;
-    }
+  int parts = sms / tail;
+  if (parts > kMaxParts) parts = kMaxParts;
+  if (parts < 2) return s;
+  s.tail = tail;
+  s.parts = parts;
+  s.done_bytes = ((size_t)tail * 4 + 255) / 256 * 256;
+  s.bytes = s.done_bytes + (size_t)tail * parts * kSlotFloats * sizeof(float);
   return s;
 }
 
@@ -843,14 +887,20 @@ cudaError_t launch_sparse_attn(const SparseArgs& a, int* drv_err, cudaStream_t s
       p.n_main = units - sp.tail;
       p.parts = sp.parts;
       grid = p.n_main + sp.tail * sp.parts;
-      ea = cudaMemsetAsync(p.done, 0, (size_t)sp.tail * 4, stream);
-      if (ea != cudaSuccess) return ea;
+      if (sp.parts <= kKernelMergeParts) {  // the last part to finish merges
+        ea = cudaMemsetAsync(p.done, 0, (size_t)sp.tail * 4, stream);
+        if (ea != cudaSuccess) return ea;
+      }
     }
   }
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   sparse_attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kvmap, outmap, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.parts <= kKernelMergeParts) return e;
+  const int tail = (grid - p.n_main) / p.parts;
+  sparse_merge_kernel<<<tail * (kHeads / kMergeHeads), kMergeThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
