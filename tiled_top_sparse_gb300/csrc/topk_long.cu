@@ -287,9 +287,11 @@ __global__ void __launch_bounds__(kLThreads, 3) topk_long_compact_kernel(
 // descending key order; a counting pass and a scan place every bucket, the buckets that
 // start before `take` are filled (atomic cursors: any order inside a bucket), and each
 // member's output place is its bucket's start plus the number of larger composites in
-// its bucket. Buckets hold a value's ties (the row's many copies of one bf16 value, ~20
-// among the picks of a normal row), so the comparisons stay few; a selectable bucket of
-// more than kFMaxBucket members sends the row to the radix select and bitonic sort.
+// its bucket. A bucket holds at least a value's ties (up to ~90 copies of one bf16 value
+// among the picks of a normal row); when the keys take fewer than 256 values, each value
+// gets 16 buckets, one per sixteenth of the window in position order, so the
+// comparisons stay few. A selectable bucket of more than kFMaxBucket members sends the
+// row to the radix select and bitonic sort.
 constexpr int kFBuckets = 4096;
 constexpr int kFBucketBits = 12;
 constexpr uint32_t kFMaxBucket = 512;
