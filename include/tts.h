@@ -8,7 +8,9 @@
  *   current CUDA device; sizes and scalars are host values. The caller owns
  *   all memory. The library allocates nothing and keeps no state between
  *   calls except cached driver entry points and, per device, the number of
- *   CTA pairs tts_qkv_rope can keep resident (queried on its first call).
+ *   CTA pairs tts_qkv_rope can keep resident (queried on its first call) and
+ *   the largest shared-memory limit tts_topk_select has set on its kernels
+ *   (a launch refused after a context reset sets it again).
  *   One exception: tts_attn_fwd_varlen_f32_noalloc (end of this file) uses a
  *   fixed TTS_NOALLOC_SCRATCH_BYTES array of device memory that the library
  *   itself holds on every GPU that loads it, and caches that array's address
